@@ -1,0 +1,386 @@
+"""Decode-step benchmark: KV append + paged decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch: the KV append of the
+step's new tokens (wllm_reshape_and_cache) followed by paged decode attention
+for every sequence (wllm_paged_attention_decode), both through the C ABI.
+Inputs are seeded synthetic decode steps (paged_kv_cache_185_gb300.workloads),
+resident in HBM when timing starts.  L2 is flushed (a 512 MiB write) between
+timed steps, outside the timed events.  Every step is timed with CUDA events on
+the launching stream; per-kernel durations come from events around each launch.
+
+Metric: decode-attention tokens/s (each sequence advances one token per step),
+with the achieved HBM GB/s of the step and of the decode kernel (algorithmic
+bytes: unique K/V bytes read + q + out + block-table entries + lengths).
+
+With N > 1 (torchrun), every rank runs its own replica of the workload with its
+own seed (sequences are independent: no collective on the data path); rank 0
+prints one JSON line with the whole-job tokens/s over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on the host cores, on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_185_gb300 import workloads  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+WORKLOAD_DESC = {
+    "c0": "4 seqs L={7,16,33,50}, 4/2 heads, D 64, fp32",
+    "c1": "64 seqs L~U[128,2048], 32/4 heads, D 64, fp16",
+    "c2": "128 seqs L~U[1024,4096], 32/32 heads, D 128, bf16, 128 appends to free slots",
+    "c3": "256 seqs in groups of 8 sharing 64 blocks, tails lognormal(1500, 0.5), 28/4 heads, D 128, bf16",
+    "c4": "8 seqs L~U[32768,131072], 32/8 heads, D 128, bf16, ~120 GB pool, 1% keys x8",
+}
+DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_185_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from an ncu capture (profiles/decode_traffic.txt),
+    used only while the kernel sources still hash to the captured version."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_sources_sha()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(x.split("=", 1) for x in line.split())
+            if kv.get("workload") == workload and kv.get("sources_sha") == sha:
+                return int(kv["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [ln.strip().split(", ") for ln in f if ln.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for name, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def setup_dist(gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def all_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_case(workload: str, rank: int):
+    """Rank r's replica: the named workload recipe with its own seed."""
+    return workloads.make_case(workload, replica=rank)
+
+
+def cpu_oracle_rate(case, budget_s: float, max_seqs=None):
+    """Oracle decode (after its own append) on the host cores over a bounded
+    sample of sequences; returns (tokens/s, sample description, threads)."""
+    import oracle
+    kc, vc = case.pool("cpu")
+    oracle.reshape_and_cache(case.key, case.value, kc, vc, case.slot_mapping)
+    threads = oracle.max_threads()
+    B, Hq = case.num_seqs, case.num_q_heads
+    # calibrate on one sequence, then size the sample to the budget
+    t0 = time.perf_counter()
+    oracle.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.num_kv_heads,
+                        case.scale, rows=list(range(Hq)))
+    per_seq = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(B, max(1, budget_s / per_seq)))
+    if max_seqs is not None:
+        n = min(n, max_seqs)
+    rows = list(range(n * Hq))
+    t0 = time.perf_counter()
+    oracle.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.num_kv_heads,
+                        case.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    return n / dt, f"first {n} of {B} sequences of the workload, all {Hq} heads, one decode", threads
+
+
+def run_reference(args):
+    rank, world, _ = setup_dist(args.gpus)
+    if rank != 0:
+        return
+    case = workloads.make_case(args.workload)
+    import oracle
+    kc, vc = case.pool("cpu")
+    oracle.reshape_and_cache(case.key, case.value, kc, vc, case.slot_mapping)
+    Hq = case.num_q_heads
+    t0 = time.perf_counter()
+    oracle.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens, case.num_kv_heads,
+                        case.scale, rows=list(range(Hq)))
+    per_seq = max(time.perf_counter() - t0, 1e-6)
+    budget = 90.0 / max(1, args.steps + args.warmup)  # whole run within ~1.5 min
+    n = int(min(case.num_seqs, max(1, budget / per_seq)))
+    rows = list(range(n * Hq))
+    for _ in range(args.warmup):
+        oracle.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens,
+                            case.num_kv_heads, case.scale, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.paged_decode(case.q, kc, vc, case.block_tables, case.context_lens,
+                            case.num_kv_heads, case.scale, rows=rows)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n / (ms / 1e3)
+    sample = f"first {n} of {case.num_seqs} sequences, all {Hq} heads, per step"
+    line = {
+        "impl": "reference", "metric": "decode-attn tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(case, args.workload, None),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(case, workload, part_tokens):
+    return {
+        "workload": case.name, "shape": WORKLOAD_DESC.get(workload, workload),
+        "batch": case.num_seqs, "q_heads": case.num_q_heads, "kv_heads": case.num_kv_heads,
+        "head_dim": case.head_dim, "block_size": case.block_size, "num_blocks": case.num_blocks,
+        "context_tokens": int(case.context_lens.sum()), "unique_kv_tokens": case.meta["unique_tokens"],
+        "appended_tokens": int(case.slot_mapping.numel()), "partition_tokens": part_tokens,
+        "l2": "flushed between timed steps (512 MiB write, outside the timed events)",
+    }
+
+
+def run_ours(args):
+    import paged_kv_cache_185_gb300 as wllm
+    from paged_kv_cache_185_gb300 import build as wbuild
+    rank, world, local = setup_dist(args.gpus)
+    assert torch.cuda.is_available(), "bench needs a CUDA device"
+    torch.cuda.set_device(local)
+    if rank == 0:
+        wbuild.build()
+    barrier(world)
+    wllm.load_library()
+    dev = torch.device("cuda", local)
+
+    case = replica_case(args.workload, rank)
+    B, Hq, Hkv, D, bs = case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
+    kc, vc = case.pool(dev)
+    q = case.q.to(dev)
+    key, value, slots = case.key.to(dev), case.value.to(dev), case.slot_mapping.to(dev)
+    bt, cl = case.block_tables.to(dev), case.context_lens.to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    part_tokens = wllm.partition_tokens(B, Hq, Hkv, D, case.max_blocks, bs, case.dtype)
+
+    def step():
+        wllm.reshape_and_cache(key, value, kc, vc, slots)
+        wllm.paged_attention_decode(out, q, kc, vc, bt, cl, Hkv, case.scale, bs)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            wllm.reshape_and_cache(key, value, kc, vc, slots)
+            ev[i][1].record(stream)
+            wllm.paged_attention_decode(out, q, kc, vc, bt, cl, Hkv, case.scale, bs)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_per_step = sum(step_ms) / K
+    ms_max = all_max(ms_per_step, world)
+    value = B * world / (ms_max / 1e3)
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, append + decode, D2H of the output, all inside the events
+    h_in = {n: t.pin_memory() for n, t in (("q", case.q), ("key", case.key), ("value", case.value),
+                                           ("slots", case.slot_mapping), ("bt", case.block_tables),
+                                           ("cl", case.context_lens))}
+    d_in = {"q": q, "key": key, "value": value, "slots": slots, "bt": bt, "cl": cl}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K + max(3, args.warmup)):
+        j = i - max(3, args.warmup)
+        flush.zero_()
+        if j >= 0:
+            e2e_ev[j][0].record(stream)
+        for n in d_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        wllm.decode_step(out, q, key, value, kc, vc, slots, bt, cl, Hkv, case.scale, bs)
+        h_out.copy_(out, non_blocking=True)
+        if j >= 0:
+            e2e_ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = all_max(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / K, world)
+    e2e_value = B * world / (e2e_ms / 1e3)
+
+    peak, peak_kind = measured_peak()
+    alg = case.algorithmic_bytes()
+    dec_mean = sum(dec_ms) / K
+    achieved = alg / (dec_mean / 1e3) / 1e9
+    step_bytes = alg + case.append_bytes()
+    traffic = recorded_traffic(args.workload)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, sample, threads = cpu_oracle_rate(case, budget_s=args.cpu_budget)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": "decode-attn tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[case.dtype], "data": "synthetic",
+        "config": config_of(case, args.workload, part_tokens),
+        "achieved_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
+        "pct_of_8tbs": 100.0 * step_bytes / (ms_per_step / 1e3) / 8e12,
+        "kernel_ms": {"append": sum(app_ms) / K, "decode": dec_mean,
+                      "decode_median": statistics.median(dec_ms)},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": alg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="c1", choices=list(workloads.CASE_NAMES))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

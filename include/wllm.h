@@ -1,0 +1,193 @@
+/*
+ * wllm.h -- C ABI of the GB300 paged KV-cache library (libwllm.so).
+ *
+ * Two operations make one decode step of a continuously batched engine over a
+ * paged KV cache:
+ *
+ *   wllm_reshape_and_cache       -- the KV append: scatter this step's new key
+ *                                   and value rows into the cache slots named
+ *                                   by a slot mapping;
+ *   wllm_paged_attention_decode  -- single-query attention for every running
+ *                                   sequence, reading K/V through its block
+ *                                   table from the fixed pool of physical
+ *                                   blocks.
+ *
+ * Sources (page title, then section):
+ *   "mini-vLLM" README, "How it works / Paged KV-cache": a fixed pool of
+ *     physical blocks of block_size token slots and a per-sequence block table
+ *     from logical positions to physical storage;
+ *   "mini-vLLM" README, "Results / End-to-end throughput vs baselines" (what
+ *     changed): each query head reads its KV head (grouped-query), K/V writes
+ *     are one indexed assignment per layer;
+ *   "mini-vLLM" README, "Results / Correctness": paged attention equals dense
+ *     attention over the same tokens scattered into blocks;
+ *   "wLLM" project page, "Features / Core engine": block-based KV cache with
+ *     no over-allocation, decode-time paged attention kernel.
+ *
+ * Conventions shared by every call:
+ *   - Every tensor is described by a wllm_tensor: a device pointer, an element
+ *     type, a rank and per-dimension sizes and strides counted in ELEMENTS.
+ *     The caller owns every buffer; the library never frees or keeps them.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and performs no host synchronisation, except in
+ *     check mode (environment variable WLLM_CHECK=1), where it synchronises
+ *     the stream after the launch and reports device-detected index errors.
+ *   - All argument checks run on the host before anything is launched; a
+ *     failed check returns a non-zero wllm_status, launches nothing and
+ *     records a message for wllm_last_error().
+ *   - Cache layout (both K and V): [num_blocks][num_kv_heads][block_size]
+ *     [head_dim], dense (strides D*bs*Hkv, D*bs, D, 1).  Token j of a sequence
+ *     sits in physical block table[j / block_size] at slot j % block_size; slot
+ *     number s names block s / block_size, offset s % block_size.
+ *   - Element types: q, out, key, value and both caches share one type:
+ *     WLLM_F32, WLLM_F16 or WLLM_BF16.  Accumulation is fp32 throughout; fp32
+ *     inputs never go through reduced-precision tensor-core math.
+ */
+#ifndef WLLM_H_
+#define WLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WLLM_OK = 0,
+  WLLM_ERR_INVALID_ARG = 1,  /* shape, type, stride, alignment or pointer    */
+  WLLM_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim 96)  */
+  WLLM_ERR_OUT_OF_RANGE = 3, /* check mode: an index read on the device was   */
+                             /* outside its range (slot, block id, length)    */
+  WLLM_ERR_CUDA = 4          /* a CUDA runtime call or launch failed          */
+} wllm_status;
+
+typedef enum {
+  WLLM_F32 = 0,
+  WLLM_F16 = 1,
+  WLLM_BF16 = 2,
+  WLLM_I32 = 3,
+  WLLM_I64 = 4
+} wllm_dtype;
+
+#define WLLM_MAX_DIMS 4
+
+typedef struct {
+  void* data;                      /* device pointer                         */
+  int32_t dtype;                   /* a wllm_dtype                           */
+  int32_t ndim;                    /* 1..WLLM_MAX_DIMS                       */
+  int64_t shape[WLLM_MAX_DIMS];    /* sizes; entries past ndim ignored       */
+  int64_t stride[WLLM_MAX_DIMS];   /* strides in elements                    */
+} wllm_tensor;
+
+typedef struct CUstream_st* wllm_stream; /* == cudaStream_t */
+
+/*
+ * KV append ("reshape and cache").
+ *
+ * Passage: "mini-vLLM" README, results paragraph on what changed -- the K/V
+ * write is one indexed assignment per layer, not a loop over sequences.
+ *
+ *   key, value    [T][Hkv][D]  F32/F16/BF16, last dimension contiguous, other
+ *                 strides free (e.g. a slice of a fused QKV projection output).
+ *   k_cache,
+ *   v_cache       [N_b][Hkv][bs][D] dense, same type as key.
+ *   slot_mapping  [T] WLLM_I64 (or WLLM_I32), contiguous.
+ *
+ * For every t with s = slot_mapping[t] >= 0 and every kv head h, the D stored
+ * elements of key[t][h] are copied bit for bit to k_cache[s/bs][h][s%bs], and
+ * value[t][h] to v_cache likewise.  A negative slot is padding: nothing is
+ * written.  Slots must be distinct (otherwise which copy lands is undefined).
+ * A slot >= N_b*bs is never written; in check mode the call then returns
+ * WLLM_ERR_OUT_OF_RANGE (check mode also rejects duplicate slots).
+ * T == 0 is valid and launches nothing.
+ */
+int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value,
+                           const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                           const wllm_tensor* slot_mapping, wllm_stream stream);
+
+/*
+ * Paged decode attention (one query token per sequence).
+ *
+ * Passages: "mini-vLLM" README, "How it works / Paged KV-cache" (block tables
+ * over a fixed pool) and "Results / Correctness" (equal to dense attention,
+ * grouped-query heads included); "wLLM" project page, "Features / Core engine"
+ * (custom PagedAttention kernel over a block-based KV cache).
+ *
+ *   out           [B][Hq][D]  written; same type as q; last dim contiguous.
+ *   q             [B][Hq][D]  last dimension contiguous.
+ *   k_cache,
+ *   v_cache       [N_b][Hkv][bs][D] dense, same type as q.
+ *   block_tables  [B][M_b] WLLM_I32, last dimension contiguous.  Entries past
+ *                 ceil(context_lens[b]/bs) are never read.
+ *   context_lens  [B] WLLM_I32, contiguous: tokens sequence b attends to
+ *                 (this step's appended token included), 0 <= L <= M_b*bs.
+ *   num_kv_heads  must equal the caches' Hkv; Hq % Hkv == 0.  Query head h
+ *                 reads KV head h / (Hq/Hkv).
+ *   scale         softmax scale applied to q.k (binary32), e.g. 1/sqrt(D).
+ *   block_size    must equal the caches' bs; a power of two in [8, 256].
+ *
+ * out[b][h] = sum_j softmax_j(scale * q[b][h].k_j) * v_j over j < L; a sequence
+ * with L == 0 gets zeros.  No masking, ALiBi, soft-capping or sliding window.
+ * Supported: D in {64, 128, 256}.  F16/BF16 use tensor-core QK^T and PV with
+ * fp32 accumulation; F32 uses fp32 FMA.  The cache base pointers must be
+ * 16-byte aligned.  Long contexts are split over several CTAs and combined on
+ * the device (split-KV); this uses the device workspace (see below).
+ * A block-table entry outside [0, N_b) or a length above M_b*bs is clamped on
+ * the device (the output of that sequence is then meaningless) and, in check
+ * mode, reported as WLLM_ERR_OUT_OF_RANGE.
+ */
+int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q,
+                                const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                                const wllm_tensor* block_tables,
+                                const wllm_tensor* context_lens, int num_kv_heads,
+                                float scale, int block_size, wllm_stream stream);
+
+/*
+ * Bytes of device workspace that wllm_paged_attention_decode needs for these
+ * sizes (0 when no sequence is split).  The workspace holds the split-KV
+ * partial results and one arrival counter per (sequence, kv head, head tile).
+ */
+size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int max_blocks_per_seq,
+                                            int block_size);
+
+/*
+ * Give the library a caller-owned device workspace for the current device
+ * (ptr == NULL, bytes == 0 returns to the library-owned one).  The region must
+ * stay valid until replaced; it is zeroed here (synchronously).  With a large
+ * enough workspace set, decode calls allocate nothing.  Without one, the
+ * library allocates its own on first need (cudaMalloc, synchronous) and grows
+ * it when a call needs more.  Calls that share a workspace must be ordered on
+ * the GPU (same stream, or synchronised): concurrent decode calls on different
+ * streams race on it.
+ */
+int wllm_set_workspace(void* ptr, size_t bytes);
+
+/*
+ * Split-KV partition size (tokens per CTA) the library would pick for these
+ * sizes on the current device; a multiple of 64.  The environment variable
+ * WLLM_PARTITION_TOKENS overrides the choice.  Returns -1 on invalid sizes.
+ */
+int wllm_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int max_blocks_per_seq, int block_size, int dtype);
+
+/*
+ * Read and clear the device error word of the current device: bit 0 slot out
+ * of range, bit 1 block id out of range, bit 2 context length out of range,
+ * bit 3 duplicate slot (check mode), bit 4 a bounded wait on a copy timed out.
+ * Synchronises the device.  Returns -1 if it could not be read.
+ */
+int wllm_device_errors(void);
+
+/* Thread-local message for the last call that did not return WLLM_OK. */
+const char* wllm_last_error(void);
+
+/* Library version string. */
+const char* wllm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WLLM_H_ */

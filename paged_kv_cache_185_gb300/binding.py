@@ -1,0 +1,170 @@
+"""ctypes binding over libwllm.so (C ABI in include/wllm.h).
+
+Argument marshalling only: each call turns torch tensors into ``wllm_tensor``
+descriptors (device pointer, dtype code, sizes, strides in elements), passes
+the current CUDA stream, and raises ``WllmError`` on a non-zero status.  Every
+step of the computation runs in the library's CUDA kernels; there is no CPU
+path.  Loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libwllm.so")
+
+WLLM_OK, WLLM_ERR_INVALID_ARG, WLLM_ERR_UNSUPPORTED, WLLM_ERR_OUT_OF_RANGE, WLLM_ERR_CUDA = range(5)
+_DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3, torch.int64: 4}
+
+# every symbol include/wllm.h declares
+EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode",
+            "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
+            "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version")
+
+
+class WllmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"wllm status {status}: {message}")
+        self.status = status
+
+
+class WllmTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libwllm.so (raises if it is missing: build it with ``build()`` first)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: run `python -m paged_kv_cache_185_gb300.build`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.POINTER(WllmTensor)
+        lib.wllm_reshape_and_cache.argtypes = [P, P, P, P, P, ctypes.c_void_p]
+        lib.wllm_reshape_and_cache.restype = ctypes.c_int
+        lib.wllm_paged_attention_decode.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
+                                                    ctypes.c_int, ctypes.c_void_p]
+        lib.wllm_paged_attention_decode.restype = ctypes.c_int
+        lib.wllm_paged_attention_workspace_bytes.argtypes = [ctypes.c_int] * 6
+        lib.wllm_paged_attention_workspace_bytes.restype = ctypes.c_size_t
+        lib.wllm_set_workspace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+        lib.wllm_set_workspace.restype = ctypes.c_int
+        lib.wllm_partition_tokens.argtypes = [ctypes.c_int] * 7
+        lib.wllm_partition_tokens.restype = ctypes.c_int
+        lib.wllm_device_errors.argtypes = []
+        lib.wllm_device_errors.restype = ctypes.c_int
+        lib.wllm_last_error.argtypes = []
+        lib.wllm_last_error.restype = ctypes.c_char_p
+        lib.wllm_version.argtypes = []
+        lib.wllm_version.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def describe(t: torch.Tensor) -> WllmTensor:
+    if t.dim() > 4:
+        raise ValueError("at most 4 dims")
+    d = WllmTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPE[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream_handle(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(rc: int) -> None:
+    if rc != WLLM_OK:
+        raise WllmError(rc, load_library().wllm_last_error().decode())
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (the library has no CPU path)")
+    dev = ts[0].device
+    for t in ts:
+        if t.device != dev:
+            raise ValueError("all tensors must be on one device")
+    return dev
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping) -> None:
+    """KV append: scatter key/value [T,Hkv,D] into caches [N_b,Hkv,bs,D] at ``slot_mapping``."""
+    dev = _require_cuda(key, value, k_cache, v_cache, slot_mapping)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (key, value, k_cache, v_cache, slot_mapping)]
+        _check(lib.wllm_reshape_and_cache(*[ctypes.byref(a) for a in args], _stream_handle(dev)))
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
+                           num_kv_heads: int, scale: float, block_size: int) -> torch.Tensor:
+    """Paged decode attention into ``out`` [B,Hq,D]; returns ``out``."""
+    dev = _require_cuda(out, q, k_cache, v_cache, block_tables, context_lens)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (out, q, k_cache, v_cache, block_tables, context_lens)]
+        _check(lib.wllm_paged_attention_decode(*[ctypes.byref(a) for a in args], int(num_kv_heads),
+                                               float(scale), int(block_size), _stream_handle(dev)))
+    return out
+
+
+def decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens,
+                num_kv_heads: int, scale: float, block_size: int) -> torch.Tensor:
+    """One decode step of one layer: append this step's K/V, then attend."""
+    if slot_mapping.numel() > 0:
+        reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)
+    return paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
+                                  num_kv_heads, scale, block_size)
+
+
+def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) -> int:
+    return int(load_library().wllm_paged_attention_workspace_bytes(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size))
+
+
+def set_workspace(buf: torch.Tensor | None) -> None:
+    """Use a caller-owned device buffer (uint8, 256-byte aligned) as workspace; None reverts."""
+    lib = load_library()
+    if buf is None:
+        _check(lib.wllm_set_workspace(None, 0))
+    else:
+        with torch.cuda.device(buf.device):
+            _check(lib.wllm_set_workspace(buf.data_ptr(), buf.numel() * buf.element_size()))
+
+
+def partition_tokens(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                     dtype: torch.dtype) -> int:
+    return int(load_library().wllm_partition_tokens(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                    max_blocks_per_seq, block_size, _DTYPE[dtype]))
+
+
+def device_errors() -> int:
+    return int(load_library().wllm_device_errors())
+
+
+def version() -> str:
+    return load_library().wllm_version().decode()

@@ -1,0 +1,550 @@
+// api.cu -- the C ABI of libwllm (declared in include/wllm.h): argument
+// validation, per-device state (error word, split-KV workspace), TMA tensor
+// maps over the KV pools, variant and partition choice, and the launches.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+#include <string>
+
+#include "launch.h"
+#include "wllm.h"
+
+namespace wllm {
+int launch_decode_bf16(int, DecodeVariant, int, const CUtensorMap&, const CUtensorMap&,
+                       const DecodeParams&, cudaStream_t);
+int launch_decode_f16(int, DecodeVariant, int, const CUtensorMap&, const CUtensorMap&,
+                      const DecodeParams&, cudaStream_t);
+int launch_decode_f32(int, DecodeVariant, int, const CUtensorMap&, const CUtensorMap&,
+                      const DecodeParams&, cudaStream_t);
+int smem_decode_bf16(int, DecodeVariant, int);
+int smem_decode_f16(int, DecodeVariant, int);
+int smem_decode_f32(int, DecodeVariant, int);
+int threads_decode_bf16(int);
+int threads_decode_f16(int);
+int threads_decode_f32(int);
+
+int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v) {
+  if (v == DecodeVariant::kFma || dtype == WLLM_F32) return 8;
+  // two 8-head n-tiles when a group needs them and registers allow (D <= 128)
+  return (group > 8 && head_dim <= 128) ? 16 : 8;
+}
+
+int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& kmap,
+                  const CUtensorMap& vmap, const DecodeParams& p, cudaStream_t stream) {
+  switch (dtype) {
+    case WLLM_BF16: return launch_decode_bf16(head_dim, v, p.head_tile, kmap, vmap, p, stream);
+    case WLLM_F16: return launch_decode_f16(head_dim, v, p.head_tile, kmap, vmap, p, stream);
+    case WLLM_F32: return launch_decode_f32(head_dim, DecodeVariant::kFma, p.head_tile, kmap, vmap, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int decode_smem_bytes(int dtype, int head_dim, DecodeVariant v, int head_tile) {
+  switch (dtype) {
+    case WLLM_BF16: return smem_decode_bf16(head_dim, v, head_tile);
+    case WLLM_F16: return smem_decode_f16(head_dim, v, head_tile);
+    case WLLM_F32: return smem_decode_f32(head_dim, DecodeVariant::kFma, head_tile);
+    default: return -1;
+  }
+}
+
+int decode_threads(int dtype, int head_dim) {
+  switch (dtype) {
+    case WLLM_BF16: return threads_decode_bf16(head_dim);
+    case WLLM_F16: return threads_decode_f16(head_dim);
+    case WLLM_F32: return threads_decode_f32(head_dim);
+    default: return -1;
+  }
+}
+}  // namespace wllm
+
+using namespace wllm;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(WLLM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int* err = nullptr;               // device error word
+  uint8_t* ws = nullptr;            // split-KV workspace
+  size_t ws_bytes = 0;
+  bool ws_owned = true;
+  size_t counter_bytes = 0;         // leading bytes reserved for arrival counters (kept zero)
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+}
+
+long long env_int(const char* name, long long dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || v[0] == '\0') return dflt;
+  return std::strtoll(v, nullptr, 10);
+}
+
+// Current device's state, created on first use (error word allocated and zeroed).
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(WLLM_ERR_UNSUPPORTED, "device index %d too large", dev);
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaMalloc(reinterpret_cast<void**>(&s.err), 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+    e = cudaMemset(s.err, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    s.ready = true;
+  }
+  *out = &s;
+  return WLLM_OK;
+}
+
+// Read and clear the error word after synchronising `stream`.
+int collect_device_errors(DeviceState* s, cudaStream_t stream, const char* op) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+  if (word != 0) {
+    cudaMemset(s->err, 0, sizeof word);
+    return fail(WLLM_ERR_OUT_OF_RANGE, "%s: device index check failed (error bits 0x%x)", op, word);
+  }
+  return WLLM_OK;
+}
+
+int elt_size(int dtype) {
+  switch (dtype) {
+    case WLLM_F32: return 4;
+    case WLLM_F16: return 2;
+    case WLLM_BF16: return 2;
+    case WLLM_I32: return 4;
+    case WLLM_I64: return 8;
+    default: return 0;
+  }
+}
+
+bool is_float(int dtype) { return dtype == WLLM_F32 || dtype == WLLM_F16 || dtype == WLLM_BF16; }
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int64_t x) {
+  int r = 0;
+  while ((int64_t(1) << r) < x) ++r;
+  return r;
+}
+
+int64_t numel(const wllm_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+int check_desc(const wllm_tensor* t, const char* name, int ndim) {
+  if (t == nullptr) return fail(WLLM_ERR_INVALID_ARG, "%s: null descriptor", name);
+  if (t->ndim != ndim) return fail(WLLM_ERR_INVALID_ARG, "%s: expected %d dims, got %d", name, ndim, t->ndim);
+  if (elt_size(t->dtype) == 0) return fail(WLLM_ERR_INVALID_ARG, "%s: unknown dtype %d", name, t->dtype);
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0) return fail(WLLM_ERR_INVALID_ARG, "%s: negative size in dim %d", name, i);
+  if (t->data == nullptr && numel(t) > 0) return fail(WLLM_ERR_INVALID_ARG, "%s: null data pointer", name);
+  return WLLM_OK;
+}
+
+bool contiguous(const wllm_tensor* t) {
+  int64_t expect = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->stride[i] != expect) return false;
+    expect *= t->shape[i];
+  }
+  return true;
+}
+
+bool same_shape(const wllm_tensor* a, const wllm_tensor* b) {
+  if (a->ndim != b->ndim) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i]) return false;
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// --- TMA descriptors ---------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 3-D view {D, Hkv*bs, N_b} of a [N_b][Hkv][bs][D] pool; one box is 128 bytes
+// of a row by min(bs, 16) rows, 128-byte swizzled.
+int make_pool_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blocks, int64_t hkv,
+                  int64_t bs, int64_t d, const char* name) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(WLLM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const int elt = elt_size(dtype);
+  CUtensorMapDataType dt = dtype == WLLM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : dtype == WLLM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv * bs),
+                        static_cast<cuuint64_t>(num_blocks)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elt), static_cast<cuuint64_t>(hkv * bs * d * elt)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(bs < 16 ? bs : 16), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WLLM_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return WLLM_OK;
+}
+
+// --- split-KV sizing -----------------------------------------------------------
+int choose_partition_tokens(int64_t num_seqs, int64_t num_kv_heads, int64_t head_tiles, int64_t max_blocks,
+                            int64_t block_size, int num_sms) {
+  const int64_t tokens_max = max_blocks * block_size > 0 ? max_blocks * block_size : 1;
+  long long forced = env_int("WLLM_PARTITION_TOKENS", 0);
+  int64_t P;
+  if (forced > 0) {
+    P = (forced + 63) / 64 * 64;
+  } else {
+    // largest power of two in [128, 16384] that still gives >= 64 CTAs per SM
+    // when every sequence is as long as the table allows
+    const int64_t target = 64LL * (num_sms > 0 ? num_sms : 148);
+    P = 128;
+    for (int64_t cand = 16384; cand >= 128; cand >>= 1) {
+      const int64_t units = num_seqs * num_kv_heads * head_tiles * ((tokens_max + cand - 1) / cand);
+      if (units >= target) {
+        P = cand;
+        break;
+      }
+    }
+  }
+  while ((tokens_max + P - 1) / P > 65535) P *= 2;  // grid.y limit
+  return static_cast<int>(P);
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char* wllm_last_error(void) { return g_last_error.c_str(); }
+
+const char* wllm_version(void) { return "wllm-gb300 0.1.0 (sm_103a)"; }
+
+int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
+                           const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, wllm_stream stream) {
+  int rc;
+  if ((rc = check_desc(key, "key", 3)) || (rc = check_desc(value, "value", 3)) ||
+      (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
+      (rc = check_desc(slot_mapping, "slot_mapping", 1)))
+    return rc;
+  const int dt = key->dtype;
+  if (!is_float(dt)) return fail(WLLM_ERR_INVALID_ARG, "key: dtype must be F32, F16 or BF16");
+  if (value->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
+    return fail(WLLM_ERR_INVALID_ARG, "key, value and caches must share one dtype");
+  if (slot_mapping->dtype != WLLM_I64 && slot_mapping->dtype != WLLM_I32)
+    return fail(WLLM_ERR_INVALID_ARG, "slot_mapping: dtype must be I64 or I32");
+  if (!same_shape(key, value)) return fail(WLLM_ERR_INVALID_ARG, "key and value shapes differ");
+  if (!same_shape(k_cache, v_cache)) return fail(WLLM_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  const int64_t T = key->shape[0], hkv = key->shape[1], d = key->shape[2];
+  const int64_t nb = k_cache->shape[0], bs = k_cache->shape[2];
+  if (k_cache->shape[1] != hkv || k_cache->shape[3] != d)
+    return fail(WLLM_ERR_INVALID_ARG, "cache shape [%lld,%lld,%lld,%lld] does not match key [T,%lld,%lld]",
+                (long long)nb, (long long)k_cache->shape[1], (long long)bs, (long long)k_cache->shape[3],
+                (long long)hkv, (long long)d);
+  if (!contiguous(k_cache) || !contiguous(v_cache)) return fail(WLLM_ERR_INVALID_ARG, "caches must be dense");
+  if (slot_mapping->shape[0] != T) return fail(WLLM_ERR_INVALID_ARG, "slot_mapping must have T entries");
+  if (T > 1 && slot_mapping->stride[0] != 1) return fail(WLLM_ERR_INVALID_ARG, "slot_mapping must be contiguous");
+  if (d > 1 && (key->stride[2] != 1 || value->stride[2] != 1))
+    return fail(WLLM_ERR_INVALID_ARG, "key/value last dimension must be contiguous");
+  if (!is_pow2(bs)) return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld is not a power of two", (long long)bs);
+  if (T > INT32_MAX || hkv > INT32_MAX || d * elt_size(dt) > INT32_MAX)
+    return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  if (T == 0 || hkv == 0 || d == 0) return WLLM_OK;
+
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s))) return rc;
+  const int elt = elt_size(dt);
+  AppendParams p{};
+  p.key = static_cast<const uint8_t*>(key->data);
+  p.value = static_cast<const uint8_t*>(value->data);
+  p.k_cache = static_cast<uint8_t*>(k_cache->data);
+  p.v_cache = static_cast<uint8_t*>(v_cache->data);
+  p.slots = slot_mapping->data;
+  p.slots_are_i64 = slot_mapping->dtype == WLLM_I64;
+  p.num_tokens = static_cast<int>(T);
+  p.num_kv_heads = static_cast<int>(hkv);
+  p.row_bytes = static_cast<int>(d * elt);
+  p.key_st = key->stride[0] * elt;
+  p.key_sh = key->stride[1] * elt;
+  p.val_st = value->stride[0] * elt;
+  p.val_sh = value->stride[1] * elt;
+  p.log2_bs = ilog2(bs);
+  p.num_slots = nb * bs;
+  p.vec16 = (p.row_bytes % 16 == 0) && aligned(p.key, 16) && aligned(p.value, 16) && aligned(p.k_cache, 16) &&
+            aligned(p.v_cache, 16) && p.key_st % 16 == 0 && p.key_sh % 16 == 0 && p.val_st % 16 == 0 &&
+            p.val_sh % 16 == 0;
+  if (!p.vec16 && !(aligned(p.key, 2) && aligned(p.value, 2)))
+    return fail(WLLM_ERR_INVALID_ARG, "key/value must be at least 2-byte aligned");
+  p.err = s->err;
+
+  const bool check = env_flag("WLLM_CHECK");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (check) {
+    cudaError_t e = static_cast<cudaError_t>(launch_check_append(p.slots, p.slots_are_i64, p.num_tokens,
+                                                                 p.num_slots, s->err, st));
+    if (e != cudaSuccess) return cuda_fail(e, "check_append launch");
+    if ((rc = collect_device_errors(s, st, "reshape_and_cache"))) return rc;
+  }
+  cudaError_t e = static_cast<cudaError_t>(launch_append(p, st));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  if (check) return collect_device_errors(s, st, "reshape_and_cache");
+  return WLLM_OK;
+}
+
+size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                            int max_blocks_per_seq, int block_size) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq < 0 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  DeviceState* s = nullptr;
+  const int sms = device_state(&s) == WLLM_OK ? s->num_sms : 148;
+  const int64_t group = num_q_heads / num_kv_heads;
+  const int64_t tiles = (group + 7) / 8;  // the largest tile count any variant uses
+  const int P = choose_partition_tokens(num_seqs, num_kv_heads, tiles, max_blocks_per_seq, block_size, sms);
+  const int64_t tokens_max = std::max<int64_t>(1, int64_t(max_blocks_per_seq) * block_size);
+  const int64_t parts = (tokens_max + P - 1) / P;
+  if (parts <= 1) return 0;
+  const size_t counters = align256(size_t(num_seqs) * num_kv_heads * tiles * sizeof(int));
+  const size_t partials = align256(size_t(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float));
+  return counters + partials;
+}
+
+int wllm_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                          int block_size, int dtype) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+      block_size <= 0 || max_blocks_per_seq < 0 || !is_float(dtype))
+    return -1;
+  DeviceState* s = nullptr;
+  const int sms = device_state(&s) == WLLM_OK ? s->num_sms : 148;
+  const DecodeVariant v =
+      (dtype != WLLM_F32 && !env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kMma : DecodeVariant::kFma;
+  const int group = num_q_heads / num_kv_heads;
+  const int ht = decode_head_tile(dtype, head_dim, group, v);
+  return choose_partition_tokens(num_seqs, num_kv_heads, (group + ht - 1) / ht, max_blocks_per_seq, block_size,
+                                 sms);
+}
+
+int wllm_set_workspace(void* ptr, size_t bytes) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc) return rc;
+  if ((ptr == nullptr) != (bytes == 0)) return fail(WLLM_ERR_INVALID_ARG, "ptr and bytes must be both set or both 0");
+  if (ptr != nullptr && !aligned(ptr, 256)) return fail(WLLM_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if (s->ws_owned && s->ws != nullptr) cudaFree(s->ws);
+  s->ws = static_cast<uint8_t*>(ptr);
+  s->ws_bytes = bytes;
+  s->ws_owned = ptr == nullptr;
+  s->counter_bytes = 0;
+  if (ptr != nullptr) {
+    e = cudaMemset(ptr, 0, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+  }
+  return WLLM_OK;
+}
+
+int wllm_device_errors(void) {
+  DeviceState* s = nullptr;
+  if (device_state(&s) != WLLM_OK) return -1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  int word = 0;
+  if (cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (word != 0 && cudaMemset(s->err, 0, sizeof word) != cudaSuccess) return -1;
+  return word;
+}
+
+int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
+                                wllm_stream stream) {
+  int rc;
+  if ((rc = check_desc(out, "out", 3)) || (rc = check_desc(q, "q", 3)) ||
+      (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
+      (rc = check_desc(block_tables, "block_tables", 2)) || (rc = check_desc(context_lens, "context_lens", 1)))
+    return rc;
+  const int dt = q->dtype;
+  if (!is_float(dt)) return fail(WLLM_ERR_INVALID_ARG, "q: dtype must be F32, F16 or BF16");
+  if (out->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
+    return fail(WLLM_ERR_INVALID_ARG, "q, out and caches must share one dtype");
+  if (block_tables->dtype != WLLM_I32) return fail(WLLM_ERR_INVALID_ARG, "block_tables: dtype must be I32");
+  if (context_lens->dtype != WLLM_I32) return fail(WLLM_ERR_INVALID_ARG, "context_lens: dtype must be I32");
+  if (!same_shape(out, q)) return fail(WLLM_ERR_INVALID_ARG, "out and q shapes differ");
+  if (!same_shape(k_cache, v_cache)) return fail(WLLM_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  const int64_t B = q->shape[0], hq = q->shape[1], d = q->shape[2];
+  const int64_t nb = k_cache->shape[0], hkv = k_cache->shape[1], bs = k_cache->shape[2];
+  if (k_cache->shape[3] != d) return fail(WLLM_ERR_INVALID_ARG, "cache head_dim differs from q");
+  if (hkv != num_kv_heads)
+    return fail(WLLM_ERR_INVALID_ARG, "num_kv_heads %d differs from cache dim %lld", num_kv_heads, (long long)hkv);
+  if (bs != block_size)
+    return fail(WLLM_ERR_INVALID_ARG, "block_size %d differs from cache dim %lld", block_size, (long long)bs);
+  if (hkv <= 0 || hq % hkv != 0) return fail(WLLM_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  if (block_tables->shape[0] != B) return fail(WLLM_ERR_INVALID_ARG, "block_tables must have B rows");
+  if (context_lens->shape[0] != B) return fail(WLLM_ERR_INVALID_ARG, "context_lens must have B entries");
+  if (B > 1 && context_lens->stride[0] != 1) return fail(WLLM_ERR_INVALID_ARG, "context_lens must be contiguous");
+  const int64_t mb = block_tables->shape[1];
+  if (mb > 1 && block_tables->stride[1] != 1)
+    return fail(WLLM_ERR_INVALID_ARG, "block_tables rows must be contiguous");
+  if (!contiguous(k_cache) || !contiguous(v_cache)) return fail(WLLM_ERR_INVALID_ARG, "caches must be dense");
+  if (d > 1 && (q->stride[2] != 1 || out->stride[2] != 1))
+    return fail(WLLM_ERR_INVALID_ARG, "q/out last dimension must be contiguous");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(WLLM_ERR_INVALID_ARG, "scale must be finite");
+  if (d != 64 && d != 128 && d != 256)
+    return fail(WLLM_ERR_UNSUPPORTED, "head_dim %lld not supported (64, 128, 256)", (long long)d);
+  if (!is_pow2(bs) || bs < 8 || bs > 256)
+    return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
+  if (B > INT32_MAX || hq > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
+    return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  if (B == 0 || hq == 0) return WLLM_OK;
+  if (nb < 1) return fail(WLLM_ERR_INVALID_ARG, "the pool has no blocks");
+  if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
+    return fail(WLLM_ERR_INVALID_ARG, "cache base pointers must be 16-byte aligned");
+
+  DecodeVariant variant = (dt == WLLM_F32 || env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kFma : DecodeVariant::kMma;
+  if (variant == DecodeVariant::kMma &&
+      !(aligned(q->data, 4) && q->stride[0] % 2 == 0 && q->stride[1] % 2 == 0))
+    return fail(WLLM_ERR_INVALID_ARG, "q rows must be 4-byte aligned for the tensor-core path");
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  const int group = static_cast<int>(hq / hkv);
+  const int head_tile = decode_head_tile(dt, static_cast<int>(d), group, variant);
+  const int tiles = (group + head_tile - 1) / head_tile;
+  const int P = choose_partition_tokens(B, hkv, tiles, mb, bs, s->num_sms);
+  const int64_t tokens_max = std::max<int64_t>(1, mb * bs);
+  const int64_t parts = (tokens_max + P - 1) / P;
+  if (hkv * tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
+
+  DecodeParams p{};
+  p.out = out->data;
+  p.q = q->data;
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.o_sb = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_stride = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.num_seqs = static_cast<int>(B);
+  p.num_q_heads = static_cast<int>(hq);
+  p.num_kv_heads = static_cast<int>(hkv);
+  p.group = group;
+  p.head_tile = head_tile;
+  p.num_head_tiles = tiles;
+  p.max_blocks = static_cast<int>(mb);
+  p.block_size = static_cast<int>(bs);
+  p.log2_bs = ilog2(bs);
+  p.num_blocks = static_cast<int>(nb);
+  p.part_tokens = P;
+  p.max_parts = static_cast<int>(parts);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = s->err;
+  p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
+
+  if (parts > 1) {
+    const size_t counters = align256(size_t(B) * hkv * tiles * sizeof(int));
+    const size_t partials = align256(size_t(B) * hq * parts * (d + 2) * sizeof(float));
+    size_t reserved = std::max(s->counter_bytes, counters);
+    if (reserved + partials > s->ws_bytes) {
+      if (!s->ws_owned)
+        return fail(WLLM_ERR_INVALID_ARG, "workspace too small: %zu bytes set, %zu needed", s->ws_bytes,
+                    reserved + partials);
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+      if (s->ws != nullptr) cudaFree(s->ws);
+      s->ws = nullptr;
+      s->ws_bytes = 0;
+      s->counter_bytes = 0;
+      reserved = counters;
+      const size_t want = (reserved + partials) + (reserved + partials) / 4;
+      e = cudaMalloc(reinterpret_cast<void**>(&s->ws), want);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+      s->ws_bytes = want;
+    }
+    if (counters > s->counter_bytes) {  // extend the zeroed counter region, stream-ordered
+      cudaError_t e = cudaMemsetAsync(s->ws + s->counter_bytes, 0, counters - s->counter_bytes, st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+      s->counter_bytes = counters;
+    }
+    p.ws_count = reinterpret_cast<int*>(s->ws);
+    p.ws_ml = reinterpret_cast<float*>(s->ws + s->counter_bytes);
+    p.ws_o = p.ws_ml + align256(size_t(B) * hq * parts * 2 * sizeof(float)) / sizeof(float);
+  }
+
+  CUtensorMap kmap, vmap;
+  if ((rc = make_pool_map(&kmap, k_cache->data, dt, nb, hkv, bs, d, "k_cache"))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, dt, nb, hkv, bs, d, "v_cache"))) return rc;
+
+  const bool check = env_flag("WLLM_CHECK");
+  if (check) {
+    cudaError_t e = static_cast<cudaError_t>(launch_check_decode(p.block_tables, p.bt_stride, p.context_lens,
+                                                                 p.num_seqs, p.max_blocks, p.block_size,
+                                                                 p.num_blocks, s->err, st));
+    if (e != cudaSuccess) return cuda_fail(e, "check_decode launch");
+    if ((rc = collect_device_errors(s, st, "paged_attention_decode"))) return rc;
+  }
+  cudaError_t e = static_cast<cudaError_t>(launch_decode(dt, static_cast<int>(d), variant, kmap, vmap, p, st));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (check) return collect_device_errors(s, st, "paged_attention_decode");
+  return WLLM_OK;
+}
+
+}  // extern "C"

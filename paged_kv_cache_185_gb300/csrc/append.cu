@@ -1,0 +1,126 @@
+// append.cu -- the KV-cache append ("reshape and cache") and the check-mode
+// index validation kernels.
+//
+// Method: "mini-vLLM" README, results paragraph on what changed -- the K/V
+// write is one indexed assignment per layer rather than a loop over
+// sequences.  Here that assignment is one kernel: a warp per (token, kv head)
+// copies the token's K row and V row (head_dim elements each) into slot
+// slot_mapping[t] = physical block * block_size + offset of the cache laid out
+// [num_blocks][num_kv_heads][block_size][head_dim].  The copy moves raw bits
+// (16-byte vectors when rows and strides allow), so it is bit-exact for every
+// element type.
+#include "common.cuh"
+#include "launch.h"
+
+namespace wllm {
+
+namespace {
+
+constexpr int kAppendWarps = 8;
+
+template <bool kVec16>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+  if (gw >= static_cast<int64_t>(p.num_tokens) * p.num_kv_heads) return;
+  const int t = static_cast<int>(gw / p.num_kv_heads);
+  const int h = static_cast<int>(gw - static_cast<int64_t>(t) * p.num_kv_heads);
+  const int64_t slot = p.slots_are_i64 ? static_cast<const int64_t*>(p.slots)[t]
+                                       : static_cast<int64_t>(static_cast<const int32_t*>(p.slots)[t]);
+  if (slot < 0) return;  // padding token
+  if (slot >= p.num_slots) {
+    if (lane == 0) atomicOr(p.err, kErrSlot);
+    return;
+  }
+  const int64_t blk = slot >> p.log2_bs;
+  const int64_t off = slot & ((int64_t(1) << p.log2_bs) - 1);
+  const int64_t dst = (((blk * p.num_kv_heads + h) << p.log2_bs) + off) * p.row_bytes;
+  const uint8_t* ks = p.key + t * p.key_st + h * p.key_sh;
+  const uint8_t* vs = p.value + t * p.val_st + h * p.val_sh;
+  uint8_t* kd = p.k_cache + dst;
+  uint8_t* vd = p.v_cache + dst;
+  if constexpr (kVec16) {
+    const int n = p.row_bytes >> 4;  // 16-byte units per row
+    for (int u = lane; u < 2 * n; u += 32) {
+      if (u < n)
+        reinterpret_cast<uint4*>(kd)[u] = reinterpret_cast<const uint4*>(ks)[u];
+      else
+        reinterpret_cast<uint4*>(vd)[u - n] = reinterpret_cast<const uint4*>(vs)[u - n];
+    }
+  } else {
+    const int n = p.row_bytes >> 1;  // 2-byte units (every supported element is 2 or 4 bytes)
+    for (int u = lane; u < 2 * n; u += 32) {
+      if (u < n)
+        reinterpret_cast<uint16_t*>(kd)[u] = reinterpret_cast<const uint16_t*>(ks)[u];
+      else
+        reinterpret_cast<uint16_t*>(vd)[u - n] = reinterpret_cast<const uint16_t*>(vs)[u - n];
+    }
+  }
+}
+
+__global__ void check_decode_kernel(const int32_t* block_tables, int64_t bt_stride,
+                                    const int32_t* context_lens, int num_seqs, int max_blocks,
+                                    int block_size, int num_blocks, int* err) {
+  const int b = blockIdx.x;
+  if (b >= num_seqs) return;
+  const int L = context_lens[b];
+  if (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(max_blocks) * block_size) {
+    if (threadIdx.x == 0) atomicOr(err, kErrLen);
+    return;
+  }
+  const int used = (L + block_size - 1) / block_size;
+  for (int j = threadIdx.x; j < used; j += blockDim.x) {
+    const int e = block_tables[b * bt_stride + j];
+    if (e < 0 || e >= num_blocks) atomicOr(err, kErrBlock);
+  }
+}
+
+__global__ void check_append_kernel(const void* slots, int slots_are_i64, int num_tokens,
+                                    int64_t num_slots, int* err) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= num_tokens) return;
+  auto slot_at = [&](int i) -> int64_t {
+    return slots_are_i64 ? static_cast<const int64_t*>(slots)[i]
+                         : static_cast<int64_t>(static_cast<const int32_t*>(slots)[i]);
+  };
+  const int64_t s = slot_at(t);
+  if (s >= num_slots) atomicOr(err, kErrSlot);
+  if (s < 0) return;
+  for (int u = 0; u < t; ++u)  // quadratic, check mode only
+    if (slot_at(u) == s) {
+      atomicOr(err, kErrDupSlot);
+      break;
+    }
+}
+
+}  // namespace
+
+int launch_append(const AppendParams& p, cudaStream_t stream) {
+  const int64_t warps = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads;
+  const int64_t blocks = (warps + kAppendWarps - 1) / kAppendWarps;
+  if (blocks == 0) return cudaSuccess;
+  if (p.vec16)
+    append_kernel<true><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
+  else
+    append_kernel<false><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+int launch_check_decode(const int32_t* block_tables, int64_t bt_stride, const int32_t* context_lens,
+                        int num_seqs, int max_blocks, int block_size, int num_blocks, int* err,
+                        cudaStream_t stream) {
+  if (num_seqs == 0) return cudaSuccess;
+  check_decode_kernel<<<num_seqs, 128, 0, stream>>>(block_tables, bt_stride, context_lens, num_seqs,
+                                                    max_blocks, block_size, num_blocks, err);
+  return cudaGetLastError();
+}
+
+int launch_check_append(const void* slots, int slots_are_i64, int num_tokens, int64_t num_slots,
+                        int* err, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  check_append_kernel<<<(num_tokens + 127) / 128, 128, 0, stream>>>(slots, slots_are_i64, num_tokens,
+                                                                    num_slots, err);
+  return cudaGetLastError();
+}
+
+}  // namespace wllm

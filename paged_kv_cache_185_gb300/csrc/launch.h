@@ -1,0 +1,72 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wllm {
+
+// Everything one paged-decode launch needs besides the two tensor maps.
+struct DecodeParams {
+  void* out;                 // [B][Hq][D]
+  const void* q;             // [B][Hq][D]
+  int64_t q_sb, q_sh;        // q strides (elements) of the seq and head dims
+  int64_t o_sb, o_sh;        // out strides
+  const int32_t* block_tables;
+  int64_t bt_stride;         // elements between two sequences' tables
+  const int32_t* context_lens;
+  int num_seqs, num_q_heads, num_kv_heads, group;
+  int head_tile, num_head_tiles;  // query heads per CTA, tiles per kv head
+  int max_blocks, block_size, log2_bs, num_blocks;
+  int part_tokens, max_parts;     // split-KV partition size / count
+  float scale_log2;               // scale * log2(e)
+  float* ws_o;                    // [B*Hq][max_parts][D] unnormalised partial sums
+  float* ws_ml;                   // [B*Hq][max_parts][2] running max (log2 units), sum
+  int* ws_count;                  // [B*Hkv*num_head_tiles] arrival counters, zero between calls
+  int* err;                       // device error word
+  unsigned long long wait_limit_ns;
+};
+
+struct AppendParams {
+  const uint8_t* key;
+  const uint8_t* value;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  const void* slots;
+  int slots_are_i64;
+  int num_tokens, num_kv_heads;
+  int row_bytes;                  // head_dim * element size
+  int64_t key_st, key_sh;         // strides in bytes
+  int64_t val_st, val_sh;
+  int log2_bs;
+  int64_t num_slots;              // num_blocks * block_size
+  int vec16;                      // rows and strides allow 16-byte copies
+  int* err;
+};
+
+// Kernel variants of the decode: tensor-core (16-bit only) or fp32 FMA.
+enum class DecodeVariant { kMma, kFma };
+
+// Head tile (query heads of one KV head handled by one CTA) for a variant.
+int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v);
+
+// Launch the decode kernel; returns a cudaError_t value.
+int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& kmap,
+                  const CUtensorMap& vmap, const DecodeParams& p, cudaStream_t stream);
+
+int launch_append(const AppendParams& p, cudaStream_t stream);
+
+// Check-mode kernels: record index errors in the device error word.
+int launch_check_decode(const int32_t* block_tables, int64_t bt_stride,
+                        const int32_t* context_lens, int num_seqs, int max_blocks,
+                        int block_size, int num_blocks, int* err, cudaStream_t stream);
+int launch_check_append(const void* slots, int slots_are_i64, int num_tokens,
+                        int64_t num_slots, int* err, cudaStream_t stream);
+
+// Bytes of shared memory one decode CTA uses, and its thread count.
+int decode_smem_bytes(int dtype, int head_dim, DecodeVariant v, int head_tile);
+int decode_threads(int dtype, int head_dim);
+
+}  // namespace wllm

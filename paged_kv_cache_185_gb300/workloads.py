@@ -290,44 +290,44 @@ def custom_case(name: str, *, lens, num_q_heads: int, num_kv_heads: int, head_di
 # The five workloads.  Seeds are 1000 + index.
 # ---------------------------------------------------------------------------
 
-def _c0():
+def _c0(r=0):
     # 4 sequences, 4/2 heads, D 64, fp32, pool of 32 blocks; append 1 token each
     return custom_case("tiny_paged_decode", lens=[7, 16, 33, 50], num_q_heads=4, num_kv_heads=2,
-                       head_dim=64, block_size=16, dtype=torch.float32, seed=1000,
+                       head_dim=64, block_size=16, dtype=torch.float32, seed=1000 + 100000 * r,
                        num_blocks=32, append="tail")
 
 
-def _c1():
-    rng = np.random.default_rng(1001)
+def _c1(r=0):
+    rng = np.random.default_rng(1001 + 100000 * r)
     lens = rng.integers(128, 2048, size=64, endpoint=True)
     return custom_case("tinyllama_1.1b_decode", lens=lens, num_q_heads=32, num_kv_heads=4,
-                       head_dim=64, block_size=16, dtype=torch.float16, seed=1001, append="tail")
+                       head_dim=64, block_size=16, dtype=torch.float16, seed=1001 + 100000 * r, append="tail")
 
 
-def _c2():
-    rng = np.random.default_rng(1002)
+def _c2(r=0):
+    rng = np.random.default_rng(1002 + 100000 * r)
     lens = rng.integers(1024, 4096, size=128, endpoint=True)
     return custom_case("llama2_7b_mha_decode", lens=lens, num_q_heads=32, num_kv_heads=32,
-                       head_dim=128, block_size=16, dtype=torch.bfloat16, seed=1002,
+                       head_dim=128, block_size=16, dtype=torch.bfloat16, seed=1002 + 100000 * r,
                        spare_blocks=64, append="free", n_append=128)
 
 
-def _c3():
-    rng = np.random.default_rng(1003)
+def _c3(r=0):
+    rng = np.random.default_rng(1003 + 100000 * r)
     z = rng.standard_normal(256)
     tails = np.clip(np.rint(1500.0 * np.exp(0.5 * z)), 1, 32768 - 1024).astype(np.int64)
     lens = 1024 + tails
     return custom_case("qwen2.5_7b_gqa_prefix_decode", lens=lens, num_q_heads=28, num_kv_heads=4,
-                       head_dim=128, block_size=16, dtype=torch.bfloat16, seed=1003,
+                       head_dim=128, block_size=16, dtype=torch.bfloat16, seed=1003 + 100000 * r,
                        groups=(8, 64), append="tail")
 
 
-def _c4():
-    rng = np.random.default_rng(1004)
+def _c4(r=0):
+    rng = np.random.default_rng(1004 + 100000 * r)
     lens = rng.integers(32768, 131072, size=8, endpoint=True)
     n_b = (120 * 10**9) // (2 * 8 * 16 * 128 * 2)
     return custom_case("long_context_splitkv_decode", lens=lens, num_q_heads=32, num_kv_heads=8,
-                       head_dim=128, block_size=16, dtype=torch.bfloat16, seed=1004,
+                       head_dim=128, block_size=16, dtype=torch.bfloat16, seed=1004 + 100000 * r,
                        num_blocks=n_b, append="tail", heavy_key_frac=0.01, heavy_key_factor=8.0)
 
 
@@ -335,8 +335,9 @@ _BUILDERS = {"c0": _c0, "c1": _c1, "c2": _c2, "c3": _c3, "c4": _c4}
 CASE_NAMES = tuple(_BUILDERS)
 
 
-def make_case(name: str) -> DecodeCase:
+def make_case(name: str, replica: int = 0) -> DecodeCase:
     """One of the five workloads: c0 (tiny, fp32), c1 (TinyLlama-1.1B-shaped),
     c2 (Llama-2-7B-shaped MHA), c3 (Qwen2.5-7B-shaped GQA with shared prefixes),
-    c4 (long-context, 32K-128K tokens, ~120 GB pool)."""
-    return _BUILDERS[name]()
+    c4 (long-context, 32K-128K tokens, ~120 GB pool).  ``replica`` > 0 draws an
+    independent batch of the same recipe (another seed)."""
+    return _BUILDERS[name](replica)

@@ -1,0 +1,118 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_kv_cache_185_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wllm.h")
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wllm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    assert "wllm_reshape_and_cache" in names and "wllm_paged_attention_decode" in names
+    assert set(names) == set(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert "sm_103a" in binding.version()
+
+
+def desc(shape, dtype, data=FAKE, stride=None):
+    d = binding.WllmTensor()
+    d.data = data
+    d.dtype = binding._DTYPE[dtype]
+    d.ndim = len(shape)
+    if stride is None:
+        stride, acc = [], 1
+        for s in reversed(shape):
+            stride.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, stride)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def decode(lib, out, q, kc, vc, bt, cl, hkv=2, scale=0.125, bs=16):
+    r = lambda x: None if x is None else ctypes.byref(x)  # noqa: E731
+    return lib.wllm_paged_attention_decode(r(out), r(q), r(kc), r(vc), r(bt), r(cl), hkv, scale, bs, None)
+
+
+def good(B=2, Hq=4, Hkv=2, D=64, bs=16, nb=8, mb=4, dt=torch.bfloat16):
+    return dict(out=desc((B, Hq, D), dt), q=desc((B, Hq, D), dt), kc=desc((nb, Hkv, bs, D), dt),
+                vc=desc((nb, Hkv, bs, D), dt), bt=desc((B, mb), torch.int32),
+                cl=desc((B,), torch.int32))
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a: a.update(q=desc((2, 4), torch.bfloat16)), 1),                  # rank
+    (lambda a: a.update(out=desc((2, 4, 64), torch.float16)), 1),            # dtype mismatch
+    (lambda a: a.update(cl=desc((2,), torch.int64)), 1),                      # lens dtype
+    (lambda a: a.update(bt=desc((3, 4), torch.int32)), 1),                    # table rows
+    (lambda a: a.update(kc=desc((8, 2, 16, 64), torch.bfloat16, stride=(2048, 1024, 128, 1))), 1),
+    (lambda a: a.update(q=desc((2, 4, 64), torch.bfloat16, stride=(256, 64, 2)), out=desc((2, 4, 64), torch.bfloat16, stride=(256, 64, 2))), 1),
+    (lambda a: a.update(kc=None), 1),                                         # null descriptor
+    (lambda a: a.update(q=desc((2, 4, 64), torch.bfloat16, data=None)), 1),   # null data
+])
+def test_decode_rejects_bad_arguments(lib, mutate, status):
+    a = good()
+    mutate(a)
+    assert decode(lib, **a) == status
+    assert lib.wllm_last_error().decode()
+
+
+def test_decode_rejects_bad_sizes(lib):
+    assert decode(lib, **good(), hkv=3) == 1                       # kv heads mismatch
+    assert decode(lib, **good(), bs=8) == 1                        # block size mismatch
+    assert decode(lib, **good(Hq=5, Hkv=2)) != 0                   # Hq % Hkv
+    assert decode(lib, **good(D=96)) == 2                          # unsupported head_dim
+    assert decode(lib, **good(bs=4), bs=4) == 2                    # unsupported block size
+    assert decode(lib, **good(), scale=float("nan")) == 1
+    assert decode(lib, **good(B=0)) == 0                           # empty batch: nothing to do
+
+
+def test_append_rejects_bad_arguments(lib):
+    r = ctypes.byref
+    key = desc((3, 2, 64), torch.float16)
+    kc = desc((4, 2, 16, 64), torch.float16)
+    slots = desc((3,), torch.int64)
+    call = lambda k, v, c1, c2, s: lib.wllm_reshape_and_cache(r(k), r(v), r(c1), r(c2), r(s), None)  # noqa
+    assert call(desc((3, 2), torch.float16), key, kc, kc, slots) == 1
+    assert call(key, desc((3, 2, 64), torch.bfloat16), kc, kc, slots) == 1
+    assert call(key, key, kc, kc, desc((3,), torch.float32)) == 1
+    assert call(key, key, kc, kc, desc((4,), torch.int64)) == 1
+    assert call(key, key, desc((4, 3, 16, 64), torch.float16), kc, slots) == 1
+    assert call(key, key, desc((4, 2, 16, 64), torch.float16, stride=(4096, 2048, 64, 2)), kc, slots) == 1
+    assert call(key, key, desc((4, 2, 12, 64), torch.float16), desc((4, 2, 12, 64), torch.float16), slots) == 2
+    empty = desc((0, 2, 64), torch.float16)
+    assert call(empty, empty, kc, kc, desc((0,), torch.int64)) == 0
+
+
+def test_binding_refuses_host_tensors():
+    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(2, 1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.paged_attention_decode(torch.empty_like(q), q, kc, kc,
+                                       torch.zeros(1, 1, dtype=torch.int32),
+                                       torch.ones(1, dtype=torch.int32), 1, 0.1, 16)

@@ -305,7 +305,7 @@ def run_ours(args):
     dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
     ms_per_step = sum(step_ms) / K
     ms_max = all_max(ms_per_step, world)
-    value = B * world / (ms_max / 1e3)
+    tok_s = B * world / (ms_max / 1e3)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, append + decode, D2H of the output, all inside the events
@@ -345,7 +345,7 @@ def run_ours(args):
         rate, sample, threads = cpu_oracle_rate(case, budget_s=args.cpu_budget)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
     line = {
-        "metric": "decode-attn tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": "decode-attn tokens/s", "value": tok_s, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[case.dtype], "data": "synthetic",
         "config": config_of(case, args.workload, part_tokens),

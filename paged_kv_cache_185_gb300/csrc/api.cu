@@ -25,6 +25,30 @@ int smem_decode_f32(int, DecodeVariant, int);
 int threads_decode_bf16(int);
 int threads_decode_f16(int);
 int threads_decode_f32(int);
+int launch_persistent_bf16(int, int, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, bool,
+                           cudaStream_t);
+int launch_persistent_f16(int, int, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, bool,
+                          cudaStream_t);
+int occupancy_persistent_bf16(int, int, int);
+int occupancy_persistent_f16(int, int, int);
+
+int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
+                             cudaStream_t stream) {
+  switch (dtype) {
+    case WLLM_BF16:
+      return launch_persistent_bf16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, stream);
+    case WLLM_F16:
+      return launch_persistent_f16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs) {
+  return dtype == WLLM_BF16 ? occupancy_persistent_bf16(head_dim, head_tile, num_seqs)
+                            : occupancy_persistent_f16(head_dim, head_tile, num_seqs);
+}
 
 int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v) {
   if (v == DecodeVariant::kFma || dtype == WLLM_F32) return 8;
@@ -135,7 +159,7 @@ int collect_device_errors(DeviceState* s, cudaStream_t stream, const char* op) {
   e = cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
   if (word != 0) {
-    cudaMemset(s->err, 0, sizeof word);
+    cudaMemset(s->err, 0, 256);
     return fail(WLLM_ERR_OUT_OF_RANGE, "%s: device index check failed (error bits 0x%x)", op, word);
   }
   return WLLM_OK;
@@ -239,21 +263,19 @@ int make_pool_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blo
 }
 
 // --- split-KV sizing -----------------------------------------------------------
-int choose_partition_tokens(int64_t num_seqs, int64_t num_kv_heads, int64_t head_tiles, int64_t max_blocks,
-                            int64_t block_size, int num_sms) {
-  const int64_t tokens_max = max_blocks * block_size > 0 ? max_blocks * block_size : 1;
+// Grid kernel: one CTA per (sequence, partition, kv-head tile); the largest
+// power of two in [128, 16384] that still gives >= 64 CTAs per SM when every
+// sequence is as long as the table allows.
+int choose_partition_grid(int64_t num_seqs, int64_t units_per_part, int64_t tokens_max, int num_sms) {
   long long forced = env_int("WLLM_PARTITION_TOKENS", 0);
   int64_t P;
   if (forced > 0) {
     P = (forced + 63) / 64 * 64;
   } else {
-    // largest power of two in [128, 16384] that still gives >= 64 CTAs per SM
-    // when every sequence is as long as the table allows
     const int64_t target = 64LL * (num_sms > 0 ? num_sms : 148);
     P = 128;
     for (int64_t cand = 16384; cand >= 128; cand >>= 1) {
-      const int64_t units = num_seqs * num_kv_heads * head_tiles * ((tokens_max + cand - 1) / cand);
-      if (units >= target) {
+      if (num_seqs * units_per_part * ((tokens_max + cand - 1) / cand) >= target) {
         P = cand;
         break;
       }
@@ -263,7 +285,71 @@ int choose_partition_tokens(int64_t num_seqs, int64_t num_kv_heads, int64_t head
   return static_cast<int>(P);
 }
 
+// Persistent kernel: units are taken dynamically, so what matters is that a
+// unit is small against one CTA's share of the work: the largest power of two
+// in [128, 4096] giving >= 16 units per CTA when sequences are half as long as
+// the table allows (lengths are on the device; the table width is all the
+// host knows).
+int choose_partition_persistent(int64_t num_seqs, int64_t units_per_part, int64_t tokens_max, int64_t n_ctas) {
+  long long forced = env_int("WLLM_PARTITION_TOKENS", 0);
+  if (forced > 0) return static_cast<int>((forced + 15) / 16 * 16);
+  const int64_t est = tokens_max / 2 > 0 ? tokens_max / 2 : 1;
+  for (int64_t cand = 4096; cand >= 128; cand >>= 1)
+    if (num_seqs * units_per_part * ((est + cand - 1) / cand) >= 16 * n_ctas) return static_cast<int>(cand);
+  return 128;
+}
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct DecodePlan {
+  DecodeVariant variant = DecodeVariant::kMma;
+  bool persistent = false;
+  int head_tile = 8, tiles = 1, part_tokens = 0, max_parts = 1, grid = 0;
+  bool separate_combine = false;
+  size_t counter_bytes = 0, ml_bytes = 0, o_bytes = 0;  // all 0 when no sequence is split
+};
+
+bool env_is(const char* name, const char* value) {
+  const char* v = std::getenv(name);
+  return v != nullptr && std::strcmp(v, value) == 0;
+}
+
+// Variant, kernel, partition size and workspace layout of one launch over B
+// sequences.  `q_bulk_ok`: query rows are 16-byte aligned (bulk-copyable).
+DecodePlan make_plan(int dt, int64_t B, int64_t hq, int64_t hkv, int64_t d, int64_t mb, int64_t bs,
+                     bool q_bulk_ok, int num_sms) {
+  DecodePlan pl;
+  pl.variant = (dt == WLLM_F32 || env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kFma : DecodeVariant::kMma;
+  pl.persistent = pl.variant == DecodeVariant::kMma && q_bulk_ok && !env_is("WLLM_DECODE_KERNEL", "grid");
+  const int64_t group = hq / hkv;
+  pl.head_tile = decode_head_tile(dt, static_cast<int>(d), static_cast<int>(group), pl.variant);
+  pl.tiles = static_cast<int>((group + pl.head_tile - 1) / pl.head_tile);
+  const int64_t tokens_max = std::max<int64_t>(1, mb * bs);
+  const int64_t z = hkv * pl.tiles;
+  if (pl.persistent) {
+    const int occ = decode_persistent_occupancy(dt, static_cast<int>(d), pl.head_tile, static_cast<int>(B));
+    const int64_t n_ctas = int64_t(num_sms > 0 ? num_sms : 148) * occ;
+    pl.part_tokens = choose_partition_persistent(B, z, tokens_max, n_ctas);
+    pl.max_parts = static_cast<int>((tokens_max + pl.part_tokens - 1) / pl.part_tokens);
+    pl.grid = static_cast<int>(std::min<int64_t>(n_ctas, std::max<int64_t>(1, B * z * pl.max_parts)));
+    pl.separate_combine = pl.max_parts > kInKernelCombineMaxParts;
+    if (pl.max_parts > 1) {
+      pl.counter_bytes = pl.separate_combine ? 0 : align256(size_t(B) * z * kPersistentConsumers * sizeof(int));
+      pl.ml_bytes = align256(size_t(B) * hq * pl.max_parts * kPersistentConsumers * 2 * sizeof(float));
+      pl.o_bytes = align256(size_t(B) * hq * pl.max_parts * d * sizeof(float));
+    }
+  } else {
+    pl.part_tokens = choose_partition_grid(B, z, tokens_max, num_sms);
+    pl.max_parts = static_cast<int>((tokens_max + pl.part_tokens - 1) / pl.part_tokens);
+    if (pl.max_parts > 1) {
+      pl.counter_bytes = align256(size_t(B) * z * sizeof(int));
+      pl.ml_bytes = align256(size_t(B) * hq * pl.max_parts * 2 * sizeof(float));
+      pl.o_bytes = align256(size_t(B) * hq * pl.max_parts * d * sizeof(float));
+    }
+  }
+  return pl;
+}
+
 
 }  // namespace
 
@@ -351,15 +437,17 @@ size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int n
     return 0;
   DeviceState* s = nullptr;
   const int sms = device_state(&s) == WLLM_OK ? s->num_sms : 148;
-  const int64_t group = num_q_heads / num_kv_heads;
-  const int64_t tiles = (group + 7) / 8;  // the largest tile count any variant uses
-  const int P = choose_partition_tokens(num_seqs, num_kv_heads, tiles, max_blocks_per_seq, block_size, sms);
-  const int64_t tokens_max = std::max<int64_t>(1, int64_t(max_blocks_per_seq) * block_size);
-  const int64_t parts = (tokens_max + P - 1) / P;
-  if (parts <= 1) return 0;
-  const size_t counters = align256(size_t(num_seqs) * num_kv_heads * tiles * sizeof(int));
-  const size_t partials = align256(size_t(num_seqs) * num_q_heads * parts * (head_dim + 2) * sizeof(float));
-  return counters + partials;
+  // the largest need over the element types and kernels a call may use
+  size_t need = 0;
+  for (int dt : {WLLM_BF16, WLLM_F32}) {
+    for (bool bulk : {true, false}) {
+      const int64_t B = std::min<int64_t>(num_seqs, kPersistentMaxSeqs);
+      const DecodePlan pl = make_plan(dt, bulk ? B : num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_blocks_per_seq, block_size, bulk, sms);
+      need = std::max(need, pl.counter_bytes + pl.ml_bytes + pl.o_bytes);
+    }
+  }
+  return need;
 }
 
 int wllm_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
@@ -369,12 +457,9 @@ int wllm_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads, int h
     return -1;
   DeviceState* s = nullptr;
   const int sms = device_state(&s) == WLLM_OK ? s->num_sms : 148;
-  const DecodeVariant v =
-      (dtype != WLLM_F32 && !env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kMma : DecodeVariant::kFma;
-  const int group = num_q_heads / num_kv_heads;
-  const int ht = decode_head_tile(dtype, head_dim, group, v);
-  return choose_partition_tokens(num_seqs, num_kv_heads, (group + ht - 1) / ht, max_blocks_per_seq, block_size,
-                                 sms);
+  const int64_t B = std::min<int64_t>(std::max(num_seqs, 1), kPersistentMaxSeqs);
+  return make_plan(dtype, B, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size, true, sms)
+      .part_tokens;
 }
 
 int wllm_set_workspace(void* ptr, size_t bytes) {
@@ -404,9 +489,52 @@ int wllm_device_errors(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return -1;
   int word = 0;
   if (cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
-  if (word != 0 && cudaMemset(s->err, 0, sizeof word) != cudaSuccess) return -1;
+  // clearing also resets the persistent kernel's scheduler words, which an
+  // aborted launch may have left non-zero
+  if (word != 0 && cudaMemset(s->err, 0, 256) != cudaSuccess) return -1;
   return word;
 }
+
+namespace {
+
+// Point the plan's workspace regions into the device workspace, growing a
+// library-owned one when needed.  Arrival counters sit in a leading region
+// that is kept zero between calls (extended with a stream-ordered memset).
+int bind_workspace(DeviceState* s, const DecodePlan& pl, cudaStream_t st, DecodeParams& p) {
+  p.ws_count = nullptr;
+  p.ws_ml = nullptr;
+  p.ws_o = nullptr;
+  if (pl.ml_bytes == 0) return WLLM_OK;
+  const size_t partials = pl.ml_bytes + pl.o_bytes;
+  size_t reserved = std::max(s->counter_bytes, pl.counter_bytes);
+  if (reserved + partials > s->ws_bytes) {
+    if (!s->ws_owned)
+      return fail(WLLM_ERR_INVALID_ARG, "workspace too small: %zu bytes set, %zu needed", s->ws_bytes,
+                  reserved + partials);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if (s->ws != nullptr) cudaFree(s->ws);
+    s->ws = nullptr;
+    s->ws_bytes = 0;
+    s->counter_bytes = 0;
+    reserved = pl.counter_bytes;
+    const size_t want = (reserved + partials) + (reserved + partials) / 4;
+    e = cudaMalloc(reinterpret_cast<void**>(&s->ws), want);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    s->ws_bytes = want;
+  }
+  if (pl.counter_bytes > s->counter_bytes) {
+    cudaError_t e = cudaMemsetAsync(s->ws + s->counter_bytes, 0, pl.counter_bytes - s->counter_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+    s->counter_bytes = pl.counter_bytes;
+  }
+  if (pl.counter_bytes > 0) p.ws_count = reinterpret_cast<int*>(s->ws);
+  p.ws_ml = reinterpret_cast<float*>(s->ws + s->counter_bytes);
+  p.ws_o = reinterpret_cast<float*>(s->ws + s->counter_bytes + pl.ml_bytes);
+  return WLLM_OK;
+}
+
+}  // namespace
 
 int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
                                 const wllm_tensor* v_cache, const wllm_tensor* block_tables,
@@ -454,80 +582,15 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, co
   if (nb < 1) return fail(WLLM_ERR_INVALID_ARG, "the pool has no blocks");
   if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
     return fail(WLLM_ERR_INVALID_ARG, "cache base pointers must be 16-byte aligned");
-
-  DecodeVariant variant = (dt == WLLM_F32 || env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kFma : DecodeVariant::kMma;
-  if (variant == DecodeVariant::kMma &&
-      !(aligned(q->data, 4) && q->stride[0] % 2 == 0 && q->stride[1] % 2 == 0))
-    return fail(WLLM_ERR_INVALID_ARG, "q rows must be 4-byte aligned for the tensor-core path");
+  const int elt = elt_size(dt);
+  const bool q_bulk_ok = aligned(q->data, 16) && (q->stride[0] * elt) % 16 == 0 && (q->stride[1] * elt) % 16 == 0;
+  if (dt != WLLM_F32 && !(aligned(q->data, 4) && q->stride[0] % 2 == 0 && q->stride[1] % 2 == 0))
+    return fail(WLLM_ERR_INVALID_ARG, "q rows must be 4-byte aligned");
 
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState* s = nullptr;
   if ((rc = device_state(&s))) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-  const int group = static_cast<int>(hq / hkv);
-  const int head_tile = decode_head_tile(dt, static_cast<int>(d), group, variant);
-  const int tiles = (group + head_tile - 1) / head_tile;
-  const int P = choose_partition_tokens(B, hkv, tiles, mb, bs, s->num_sms);
-  const int64_t tokens_max = std::max<int64_t>(1, mb * bs);
-  const int64_t parts = (tokens_max + P - 1) / P;
-  if (hkv * tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
-
-  DecodeParams p{};
-  p.out = out->data;
-  p.q = q->data;
-  p.q_sb = q->stride[0];
-  p.q_sh = q->stride[1];
-  p.o_sb = out->stride[0];
-  p.o_sh = out->stride[1];
-  p.block_tables = static_cast<const int32_t*>(block_tables->data);
-  p.bt_stride = block_tables->stride[0];
-  p.context_lens = static_cast<const int32_t*>(context_lens->data);
-  p.num_seqs = static_cast<int>(B);
-  p.num_q_heads = static_cast<int>(hq);
-  p.num_kv_heads = static_cast<int>(hkv);
-  p.group = group;
-  p.head_tile = head_tile;
-  p.num_head_tiles = tiles;
-  p.max_blocks = static_cast<int>(mb);
-  p.block_size = static_cast<int>(bs);
-  p.log2_bs = ilog2(bs);
-  p.num_blocks = static_cast<int>(nb);
-  p.part_tokens = P;
-  p.max_parts = static_cast<int>(parts);
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.err = s->err;
-  p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
-
-  if (parts > 1) {
-    const size_t counters = align256(size_t(B) * hkv * tiles * sizeof(int));
-    const size_t partials = align256(size_t(B) * hq * parts * (d + 2) * sizeof(float));
-    size_t reserved = std::max(s->counter_bytes, counters);
-    if (reserved + partials > s->ws_bytes) {
-      if (!s->ws_owned)
-        return fail(WLLM_ERR_INVALID_ARG, "workspace too small: %zu bytes set, %zu needed", s->ws_bytes,
-                    reserved + partials);
-      cudaError_t e = cudaDeviceSynchronize();
-      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-      if (s->ws != nullptr) cudaFree(s->ws);
-      s->ws = nullptr;
-      s->ws_bytes = 0;
-      s->counter_bytes = 0;
-      reserved = counters;
-      const size_t want = (reserved + partials) + (reserved + partials) / 4;
-      e = cudaMalloc(reinterpret_cast<void**>(&s->ws), want);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-      s->ws_bytes = want;
-    }
-    if (counters > s->counter_bytes) {  // extend the zeroed counter region, stream-ordered
-      cudaError_t e = cudaMemsetAsync(s->ws + s->counter_bytes, 0, counters - s->counter_bytes, st);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
-      s->counter_bytes = counters;
-    }
-    p.ws_count = reinterpret_cast<int*>(s->ws);
-    p.ws_ml = reinterpret_cast<float*>(s->ws + s->counter_bytes);
-    p.ws_o = p.ws_ml + align256(size_t(B) * hq * parts * 2 * sizeof(float)) / sizeof(float);
-  }
 
   CUtensorMap kmap, vmap;
   if ((rc = make_pool_map(&kmap, k_cache->data, dt, nb, hkv, bs, d, "k_cache"))) return rc;
@@ -535,14 +598,57 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, co
 
   const bool check = env_flag("WLLM_CHECK");
   if (check) {
-    cudaError_t e = static_cast<cudaError_t>(launch_check_decode(p.block_tables, p.bt_stride, p.context_lens,
-                                                                 p.num_seqs, p.max_blocks, p.block_size,
-                                                                 p.num_blocks, s->err, st));
+    cudaError_t e = static_cast<cudaError_t>(launch_check_decode(
+        static_cast<const int32_t*>(block_tables->data), block_tables->stride[0],
+        static_cast<const int32_t*>(context_lens->data), static_cast<int>(B), static_cast<int>(mb),
+        static_cast<int>(bs), static_cast<int>(nb), s->err, st));
     if (e != cudaSuccess) return cuda_fail(e, "check_decode launch");
     if ((rc = collect_device_errors(s, st, "paged_attention_decode"))) return rc;
   }
-  cudaError_t e = static_cast<cudaError_t>(launch_decode(dt, static_cast<int>(d), variant, kmap, vmap, p, st));
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+
+  // the persistent kernel keeps per-sequence prefix sums in shared memory, so
+  // very large batches go in slices of kPersistentMaxSeqs sequences
+  const DecodePlan first = make_plan(dt, std::min<int64_t>(B, kPersistentMaxSeqs), hq, hkv, d, mb, bs, q_bulk_ok,
+                                     s->num_sms);
+  const int64_t slice = first.persistent ? kPersistentMaxSeqs : B;
+  for (int64_t b0 = 0; b0 < B; b0 += slice) {
+    const int64_t nbat = std::min<int64_t>(slice, B - b0);
+    const DecodePlan pl = make_plan(dt, nbat, hq, hkv, d, mb, bs, q_bulk_ok, s->num_sms);
+    DecodeParams p{};
+    p.out = static_cast<uint8_t*>(out->data) + b0 * out->stride[0] * elt;
+    p.q = static_cast<const uint8_t*>(q->data) + b0 * q->stride[0] * elt;
+    p.q_sb = q->stride[0];
+    p.q_sh = q->stride[1];
+    p.o_sb = out->stride[0];
+    p.o_sh = out->stride[1];
+    p.block_tables = static_cast<const int32_t*>(block_tables->data) + b0 * block_tables->stride[0];
+    p.bt_stride = block_tables->stride[0];
+    p.context_lens = static_cast<const int32_t*>(context_lens->data) + b0;
+    p.num_seqs = static_cast<int>(nbat);
+    p.num_q_heads = static_cast<int>(hq);
+    p.num_kv_heads = static_cast<int>(hkv);
+    p.group = static_cast<int>(hq / hkv);
+    p.head_tile = pl.head_tile;
+    p.num_head_tiles = pl.tiles;
+    p.max_blocks = static_cast<int>(mb);
+    p.block_size = static_cast<int>(bs);
+    p.log2_bs = ilog2(bs);
+    p.num_blocks = static_cast<int>(nb);
+    p.part_tokens = pl.part_tokens;
+    p.max_parts = pl.max_parts;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = s->err;
+    p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
+    if (!pl.persistent && hkv * pl.tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
+    if ((rc = bind_workspace(s, pl, st, p))) return rc;
+    cudaError_t e;
+    if (pl.persistent)
+      e = static_cast<cudaError_t>(launch_decode_persistent(dt, static_cast<int>(d), pl.head_tile, kmap, vmap, p,
+                                                            pl.grid, pl.separate_combine, st));
+    else
+      e = static_cast<cudaError_t>(launch_decode(dt, static_cast<int>(d), pl.variant, kmap, vmap, p, st));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  }
   if (check) return collect_device_errors(s, st, "paged_attention_decode");
   return WLLM_OK;
 }

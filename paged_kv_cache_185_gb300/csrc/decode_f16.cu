@@ -4,4 +4,6 @@
 #define WLLM_LAUNCH_FN launch_decode_f16
 #define WLLM_SMEM_FN smem_decode_f16
 #define WLLM_THREADS_FN threads_decode_f16
+#define WLLM_PERSIST_FN launch_persistent_f16
+#define WLLM_POCC_FN occupancy_persistent_f16
 #include "decode_dispatch.inc"

@@ -326,3 +326,58 @@ def test_empty_batch_is_a_no_op():
     key = torch.zeros(0, 2, 64, dtype=torch.bfloat16, device="cuda")
     wllm.reshape_and_cache(key, key, kc, kc, torch.zeros(0, dtype=torch.int64, device="cuda"))
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# kernel selection: persistent (default for f16/bf16) vs one-CTA-per-unit grid
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,bs", [s for s in SHAPES if s[0] != torch.float32][::2])
+def test_grid_kernel_variant(monkeypatch, dtype, Hq, Hkv, D, bs):
+    monkeypatch.setenv("WLLM_DECODE_KERNEL", "grid")
+    case = workloads.custom_case("grid", lens=LENS, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                                 block_size=bs, dtype=dtype, seed=Hq + D, spare_blocks=2)
+    got, _, _ = gpu_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, dtype, f"grid {Hq}/{Hkv} D{D} bs{bs}")
+
+
+def test_unaligned_query_rows_fall_back():
+    """q rows only 4-byte aligned: the bulk-copy path is skipped, result unchanged."""
+    case = workloads.custom_case("qalign", lens=[5, 200, 1500], num_q_heads=8, num_kv_heads=2,
+                                 head_dim=128, block_size=16, dtype=torch.bfloat16, seed=12)
+    kc, vc = case.pool("cuda")
+    wllm.reshape_and_cache(case.key.cuda(), case.value.cuda(), kc, vc, case.slot_mapping.cuda())
+    buf = torch.zeros(3, 8, 128 + 2, dtype=torch.bfloat16, device="cuda")
+    q = buf[:, :, 2:]
+    q.copy_(case.q.cuda())
+    out = torch.empty(3, 8, 128, dtype=torch.bfloat16, device="cuda")
+    wllm.paged_attention_decode(out, q, kc, vc, case.block_tables.cuda(), case.context_lens.cuda(), 2,
+                                case.scale, 16)
+    torch.cuda.synchronize()
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(out.cpu(), ref, case.dtype, "unaligned q")
+
+
+def test_large_batch_is_sliced():
+    """More sequences than one persistent launch takes (4096)."""
+    g = torch.Generator().manual_seed(13)
+    lens = torch.randint(1, 40, (4300,), generator=g).tolist()
+    case = workloads.custom_case("big", lens=lens, num_q_heads=4, num_kv_heads=1, head_dim=64,
+                                 block_size=16, dtype=torch.float16, seed=13)
+    got, _, _ = gpu_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, case.dtype, "4300 sequences")
+
+
+def test_repeated_launches_leave_scheduler_clean():
+    case = workloads.custom_case("rep", lens=[3000, 17, 900], num_q_heads=28, num_kv_heads=4,
+                                 head_dim=128, block_size=16, dtype=torch.bfloat16, seed=14)
+    first, kc, vc = gpu_step(case)
+    q = case.q.cuda()
+    for _ in range(5):
+        out = torch.empty_like(q)
+        wllm.paged_attention_decode(out, q, kc, vc, case.block_tables.cuda(), case.context_lens.cuda(),
+                                    4, case.scale, 16)
+        torch.cuda.synchronize()
+        assert torch.equal(int_view(out.cpu()), int_view(first))

@@ -286,17 +286,25 @@ int choose_partition_grid(int64_t num_seqs, int64_t units_per_part, int64_t toke
 }
 
 // Persistent kernel: units are taken dynamically, so what matters is that a
-// unit is small against one CTA's share of the work: the largest power of two
-// in [128, 4096] giving >= 16 units per CTA when sequences are half as long as
-// the table allows (lengths are on the device; the table width is all the
-// host knows).
+// unit is small against one CTA's share of the work, and that a sequence is
+// not cut into so many partitions that combining them costs more than the
+// balance gains.  The largest power of two in [256, 4096] that gives >= 16
+// units per CTA when sequences are half as long as the table allows (lengths
+// are on the device; the table width is all the host knows), but at most 128
+// partitions per sequence.  Measured on GB300 over P = 128..4096 on the
+// TinyLlama / Llama-2-7B / Qwen2.5-7B / long-context workloads.
 int choose_partition_persistent(int64_t num_seqs, int64_t units_per_part, int64_t tokens_max, int64_t n_ctas) {
   long long forced = env_int("WLLM_PARTITION_TOKENS", 0);
   if (forced > 0) return static_cast<int>((forced + 15) / 16 * 16);
   const int64_t est = tokens_max / 2 > 0 ? tokens_max / 2 : 1;
-  for (int64_t cand = 4096; cand >= 128; cand >>= 1)
-    if (num_seqs * units_per_part * ((est + cand - 1) / cand) >= 16 * n_ctas) return static_cast<int>(cand);
-  return 128;
+  int64_t P = 256;
+  for (int64_t cand = 4096; cand >= 256; cand >>= 1)
+    if (num_seqs * units_per_part * ((est + cand - 1) / cand) >= 16 * n_ctas) {
+      P = cand;
+      break;
+    }
+  while (P < 4096 && (tokens_max + P - 1) / P > 128) P *= 2;
+  return static_cast<int>(P);
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -332,10 +340,10 @@ DecodePlan make_plan(int dt, int64_t B, int64_t hq, int64_t hkv, int64_t d, int6
     pl.part_tokens = choose_partition_persistent(B, z, tokens_max, n_ctas);
     pl.max_parts = static_cast<int>((tokens_max + pl.part_tokens - 1) / pl.part_tokens);
     pl.grid = static_cast<int>(std::min<int64_t>(n_ctas, std::max<int64_t>(1, B * z * pl.max_parts)));
-    pl.separate_combine = pl.max_parts > kInKernelCombineMaxParts;
+    pl.separate_combine = pl.max_parts > kInKernelCombineMaxParts || d > 128;
     if (pl.max_parts > 1) {
-      pl.counter_bytes = pl.separate_combine ? 0 : align256(size_t(B) * z * kPersistentConsumers * sizeof(int));
-      pl.ml_bytes = align256(size_t(B) * hq * pl.max_parts * kPersistentConsumers * 2 * sizeof(float));
+      pl.counter_bytes = pl.separate_combine ? 0 : align256(size_t(B) * z * sizeof(int));
+      pl.ml_bytes = align256(size_t(B) * hq * pl.max_parts * 2 * sizeof(float));
       pl.o_bytes = align256(size_t(B) * hq * pl.max_parts * d * sizeof(float));
     }
   } else {

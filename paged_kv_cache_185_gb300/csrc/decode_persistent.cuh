@@ -12,16 +12,17 @@
 //     of a unit also carries the unit's query rows (bulk copy).  It runs
 //     ahead across unit boundaries, so the copies of the next unit are in
 //     flight while the consumers finish the current one.
-//   consumer warps (4): every consumer sees every chunk.  Each computes the
-//     full S^T = K Q^T tile with mma.sync (cheap, so done redundantly), the
-//     online-softmax update, and PV for its own quarter of head_dim; after
-//     the chunk it releases the stage.  No cross-warp merge is needed: the
-//     running max and sum are the same in every consumer warp.
+//   consumer warps (4): a stage holds 64 tokens as four 16-token sub-chunks;
+//     consumer j takes sub-chunk j: S^T = K Q^T (mma.sync m16n8k16, the GQA
+//     heads of the tile on the N side), the online-softmax update and
+//     O^T += V^T P^T over the full head_dim, keeping its own running
+//     (m, l, O).  After the sub-chunk it releases the stage.
 //
-// A unit's result is written to `out` when the sequence has one partition.
-// Otherwise each consumer warp writes its partial (m, l, O slice) to the
-// workspace; with few partitions the last warp to arrive for (b, z, quarter)
-// -- an atomic counter, never waited for -- combines them, with many a
+// At the end of a unit the consumers merge their four (m, l, O) through
+// shared memory (two rendezvous on a bounded mbarrier).  A sequence with one
+// partition gets its output written there; otherwise the merged partial goes
+// to the workspace and, with few partitions, the last CTA to arrive for
+// (b, z) -- an atomic counter, never waited for -- combines them; with many, a
 // separate combine kernel does it after the launch.
 //
 // Every wait is bounded: on timeout the warp records an error bit and leaves.
@@ -37,42 +38,44 @@ namespace wllm {
 constexpr int kSchedNextOffset = 16;
 constexpr int kSchedDoneOffset = 32;
 
-struct ChunkMeta {
+struct StageMeta {
   int b, p, t0, tok_end;
   int n_parts, h0, nh, flags;
-  int z, pad0, pad1, pad2;
+  int z, nsub, pad0, pad1;
 };
 enum : int { kFirst = 1, kLast = 2, kEmptySeq = 4, kStop = 8 };
+
+constexpr int kSub = 4;                      // 16-token sub-chunks per stage
+constexpr int kStageTokens = kSub * kChunk;  // 64 tokens per stage
 
 template <typename T, int D, int NT>
 struct PShape {
   static constexpr int kConsumers = 4;
   static constexpr int kThreads = (kConsumers + 1) * 32;
   static constexpr int kHeadTile = 8 * NT;
-  static constexpr int kKV = Geom<T, D>::kTileBytes;
+  static constexpr int kKV = Geom<T, D>::kTileBytes;  // one 16-row K (or V) sub-tile
   static constexpr int kQBytes = kHeadTile * D * static_cast<int>(sizeof(T));
-  static constexpr int kStageBytes = ((2 * kKV + kQBytes) + 1023) / 1024 * 1024;
-  static constexpr int kStages = D == 64 ? 12 : (D == 128 ? 8 : 5);
+  static constexpr int kStageBytes = ((2 * kSub * kKV + kQBytes) + 1023) / 1024 * 1024;
+  static constexpr int kRedBytes = (kConsumers * kHeadTile * (D + 2) * 4 + 127) / 128 * 128;
+  // Consumer warps, not ring depth, bound the rate (each 16-token sub-chunk is
+  // a ~1-2k-cycle dependency chain), so the target is two or three CTAs per
+  // SM (eight or more consumer warps); the ring gets what is left of the
+  // per-CTA share of shared memory after the reduction area, the
+  // per-sequence arrays (up to kPersistentMaxSeqs) and the barriers.
+  static constexpr int kCtasPerSm = D == 64 ? 3 : (D == 128 ? 2 : 1);
+  static constexpr int kSmemBudget =
+      227 * 1024 / kCtasPerSm - 1024 - 1024 - kRedBytes - (2 * kPersistentMaxSeqs + 1) * 4 - 2048;
+  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 16 ? 16 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kBarBytes = 2 * kStages * 8;
-  static constexpr int kMetaBytes = kStages * static_cast<int>(sizeof(ChunkMeta));
-  static constexpr int kFixedSmem = 1024 + kRingBytes + kBarBytes + kMetaBytes;
-  static constexpr int kMT = D / 16 / kConsumers;  // PV m-tiles (16 columns of d) per consumer
-  static constexpr int kDW = D / kConsumers;       // output columns per consumer
-  static_assert(kMT >= 1, "head_dim too small for the consumer split");
+  static constexpr int kBarBytes = (2 * kStages + 1) * 8;
+  static constexpr int kMetaBytes = kStages * static_cast<int>(sizeof(StageMeta));
+  static constexpr int kFixedSmem = 1024 + kRingBytes + kRedBytes + kBarBytes + kMetaBytes + 64;
 };
 
-// Consumer state: full-width Q^T fragments, this warp's quarter of O^T.
+// Query fragments of a unit from the stage's query rows (row stride D).
 template <typename T, int D, int NT>
-struct PState {
-  float o[PShape<T, D, NT>::kMT][NT][4];
-  float m[NT][2];
-  float l[NT][2];
-  uint32_t qb[NT][D / 16][2];
-};
-
-template <typename T, int D, int NT>
-__device__ __forceinline__ void pstate_begin(PState<T, D, NT>& st, const uint8_t* qtile, int nh, int lane) {
+__device__ __forceinline__ void load_q_smem(MmaState<T, D, NT>& st, const uint8_t* qtile, int nh, int lane) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 8 + (lane >> 2);
@@ -90,220 +93,25 @@ __device__ __forceinline__ void pstate_begin(PState<T, D, NT>& st, const uint8_t
       st.l[nt][j] = 0.f;
     }
 #pragma unroll
-    for (int i = 0; i < PShape<T, D, NT>::kMT; ++i)
+    for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) st.o[i][nt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) st.o[mt][nt][e] = 0.f;
   }
 }
 
-template <typename T, int D, int NT>
-__device__ __forceinline__ void pstate_chunk(PState<T, D, NT>& st, uint32_t k_tile, uint32_t v_tile, int t0,
-                                             int tok_end, float scale_log2, int cw, int lane) {
-  constexpr int kMT = PShape<T, D, NT>::kMT;
-  float s[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
-  const int a_row = (lane & 7) + (((lane >> 3) & 1) << 3);
-  const int a_chunk = lane >> 4;
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(k_tile + tile_offset(a_row, 2 * ks + a_chunk), a);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) Mma<T>::run(s[nt], a, st.qb[nt][ks]);
-  }
-
-  const int tok_a = t0 + (lane >> 2);
-  const bool va = tok_a < tok_end;
-  const bool vb = tok_a + 8 < tok_end;
-  float alpha[NT][2];
-  uint32_t pb[NT][2];
-  bool rescale = false;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float x0 = va ? s[nt][0] * scale_log2 : -INFINITY;
-    const float x1 = va ? s[nt][1] * scale_log2 : -INFINITY;
-    const float x2 = vb ? s[nt][2] * scale_log2 : -INFINITY;
-    const float x3 = vb ? s[nt][3] * scale_log2 : -INFINITY;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
-    }
-    const float mn0 = fmaxf(st.m[nt][0], mx0), mn1 = fmaxf(st.m[nt][1], mx1);
-    alpha[nt][0] = exp2f(st.m[nt][0] - mn0);
-    alpha[nt][1] = exp2f(st.m[nt][1] - mn1);
-    st.m[nt][0] = mn0;
-    st.m[nt][1] = mn1;
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    st.l[nt][0] = st.l[nt][0] * alpha[nt][0] + (p0 + p2);
-    st.l[nt][1] = st.l[nt][1] * alpha[nt][1] + (p1 + p3);
-    rescale |= (alpha[nt][0] != 1.f) || (alpha[nt][1] != 1.f);
-    pb[nt][0] = movmatrix_trans(Mma<T>::pack(p0, p1));
-    pb[nt][1] = movmatrix_trans(Mma<T>::pack(p2, p3));
-  }
-  if (__any_sync(kFullMask, rescale)) {
-#pragma unroll
-    for (int i = 0; i < kMT; ++i)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        st.o[i][nt][0] *= alpha[nt][0];
-        st.o[i][nt][1] *= alpha[nt][1];
-        st.o[i][nt][2] *= alpha[nt][0];
-        st.o[i][nt][3] *= alpha[nt][1];
-      }
-  }
-
-  const int v_row = (lane & 7) + ((lane >> 4) << 3);
-  const int v_chunk = (lane >> 3) & 1;
-  const bool tail = t0 + kChunk > tok_end;
-  const int tk = t0 + 2 * (lane & 3);
-  const uint32_t keep_lo = (tk < tok_end ? 0x0000ffffu : 0u) | (tk + 1 < tok_end ? 0xffff0000u : 0u);
-  const uint32_t keep_hi = (tk + 8 < tok_end ? 0x0000ffffu : 0u) | (tk + 9 < tok_end ? 0xffff0000u : 0u);
-#pragma unroll
-  for (int i = 0; i < kMT; ++i) {
-    const int mt = cw * kMT + i;
-    uint32_t a[4];
-    ldsm_x4_trans(v_tile + tile_offset(v_row, 2 * mt + v_chunk), a);
-    if (tail) {
-      a[0] &= keep_lo;
-      a[1] &= keep_lo;
-      a[2] &= keep_hi;
-      a[3] &= keep_hi;
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) Mma<T>::run(st.o[i][nt], a, pb[nt]);
-  }
-}
-
-// The split-KV partials of one (row, partition): ws_o[row][part][D] holds the
-// unnormalised O, ws_ml[row][part][consumer] the (max in log2 units, sum) pair
-// written by each consumer warp (identical values, one copy per writer so that
-// a combining warp reads only its own writers' data).
-template <typename T, int D, int NT>
-__device__ __forceinline__ void pstate_finish(PState<T, D, NT>& st, const ChunkMeta& mt_, const DecodeParams& p,
-                                              int cw, int lane) {
-  constexpr int kMT = PShape<T, D, NT>::kMT;
-  constexpr int kW = PShape<T, D, NT>::kConsumers;
-  constexpr int kDW = PShape<T, D, NT>::kDW;
-  T* out = reinterpret_cast<T*>(p.out);
-  const int b = mt_.b, h0 = mt_.h0, nh = mt_.nh;
-  if (mt_.flags & kEmptySeq) {
-    for (int idx = lane; idx < nh * kDW; idx += 32) {
-      const int hh = idx / kDW, d = cw * kDW + idx % kDW;
-      out[b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh + d] = from_f32<T>(0.f);
-    }
-    return;
-  }
-  float l[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float v = st.l[nt][j];
-      v += __shfl_xor_sync(kFullMask, v, 4);
-      v += __shfl_xor_sync(kFullMask, v, 8);
-      v += __shfl_xor_sync(kFullMask, v, 16);
-      l[nt][j] = v;
-    }
-  if (mt_.n_parts == 1) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int hh = nt * 8 + 2 * (lane & 3);
-      const float inv0 = 1.f / l[nt][0], inv1 = 1.f / l[nt][1];
-#pragma unroll
-      for (int i = 0; i < kMT; ++i) {
-        const int d = (cw * kMT + i) * 16 + (lane >> 2);
-        if (hh < nh) {
-          T* r = out + b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh;
-          r[d] = from_f32<T>(st.o[i][nt][0] * inv0);
-          r[d + 8] = from_f32<T>(st.o[i][nt][2] * inv0);
-        }
-        if (hh + 1 < nh) {
-          T* r = out + b * p.o_sb + static_cast<int64_t>(h0 + hh + 1) * p.o_sh;
-          r[d] = from_f32<T>(st.o[i][nt][1] * inv1);
-          r[d + 8] = from_f32<T>(st.o[i][nt][3] * inv1);
-        }
-      }
-    }
-    return;
-  }
-
-  // several partitions: write this warp's partial
-  const int row0 = b * p.num_q_heads + h0;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int hh = nt * 8 + 2 * (lane & 3);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (hh + j < nh) {
-        const int64_t slot = static_cast<int64_t>(row0 + hh + j) * p.max_parts + mt_.p;
-        float* wo = p.ws_o + slot * D;
-#pragma unroll
-        for (int i = 0; i < kMT; ++i) {
-          const int d = (cw * kMT + i) * 16 + (lane >> 2);
-          wo[d] = st.o[i][nt][j];
-          wo[d + 8] = st.o[i][nt][2 + j];
-        }
-        if ((lane >> 2) == 0)
-          reinterpret_cast<float2*>(p.ws_ml)[slot * kW + cw] = make_float2(st.m[nt][j], l[nt][j]);
-      }
-    }
-  }
-  if (p.ws_count == nullptr) return;  // a separate combine kernel finishes the job
-
-  __threadfence();
+// Rendezvous of the four consumer warps on an mbarrier (count 4, one arrival
+// per warp), bounded like every other wait.  `phase` counts the uses.
+__device__ __forceinline__ bool consumer_sync(uint32_t bar, int& phase, uint64_t limit_ns, int lane) {
   __syncwarp();
-  const int z = mt_.z;
-  int* counter = p.ws_count + (static_cast<int64_t>(b) * p.num_kv_heads * p.num_head_tiles + z) * kW + cw;
-  int last = 0;
-  if (lane == 0) last = atomicAdd(counter, 1) == mt_.n_parts - 1;
-  last = __shfl_sync(kFullMask, last, 0);
-  if (!last) return;
-  __threadfence();
-  const int n_parts = mt_.n_parts;
-  for (int hh = 0; hh < nh; ++hh) {
-    const int64_t base = static_cast<int64_t>(row0 + hh) * p.max_parts;
-    float M = -INFINITY;
-    for (int pp = lane; pp < n_parts; pp += 32)
-      M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (base + pp) * kW + cw).x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
-    float den = 0.f;
-    for (int pp = lane; pp < n_parts; pp += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (base + pp) * kW + cw);
-      den += exp2f(ml.x - M) * ml.y;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
-    const float inv = 1.f / den;
-    T* orow = out + b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh;
-    // lanes cover the warp's kDW columns; extra lanes take every other partition
-    constexpr int kLanesPerCol = kDW >= 32 ? 1 : 32 / kDW;
-    constexpr int kCols = kDW >= 32 ? kDW / 32 : 1;
-    const int sub = kDW >= 32 ? 0 : lane / kDW;
-#pragma unroll
-    for (int c = 0; c < kCols; ++c) {
-      const int d = cw * kDW + (kDW >= 32 ? lane + 32 * c : lane % kDW);
-      float num = 0.f;
-      for (int pp = sub; pp < n_parts; pp += kLanesPerCol) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (base + pp) * kW + cw);
-        num = fmaf(exp2f(ml.x - M), __ldcg(p.ws_o + (base + pp) * D + d), num);
-      }
-      // fold the kLanesPerCol partial sums of column d (lanes d, d + kDW, ...)
-      if constexpr (kDW < 32) {
-#pragma unroll
-        for (int off = kDW; off < 32; off <<= 1) num += __shfl_xor_sync(kFullMask, num, off);
-      }
-      if (sub == 0) orow[d] = from_f32<T>(num * inv);
-    }
-  }
-  if (lane == 0) *counter = 0;
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_bounded(bar, phase & 1, limit_ns);
+  ++phase;
+  return __all_sync(kFullMask, ok);
 }
+
+struct UnitInfo {
+  int b, part, z, n_parts, tb, te, n_chunks, kvh, h0, nh;
+};
 
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
@@ -318,17 +126,22 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PS::kRingBytes);
+  uint8_t* red_area = smem + PS::kRingBytes;  // consumers' (m, l, O) for the unit merge
+  uint64_t* full = reinterpret_cast<uint64_t*>(red_area + PS::kRedBytes);
   uint64_t* empty = full + S;
-  ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(empty + S);
-  int* prefix = reinterpret_cast<int*>(meta + S);  // [B + 1] units before sequence b
+  uint64_t* cbar = empty + S;                 // consumer rendezvous
+  StageMeta* meta = reinterpret_cast<StageMeta*>(cbar + 1);
+  int* wsum = reinterpret_cast<int*>(meta + S);  // 16 ints of scratch
+  int* last_flag = wsum;                         // reused once the prefix sums are done
+  int* prefix = wsum + 16;                       // [B + 1] units before sequence b
+  int* lens = prefix + p.num_seqs + 1;           // [B] clamped context lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.num_seqs;
   const int Z = p.num_kv_heads * p.num_head_tiles;
   const int l_max = p.max_blocks * p.block_size;
 
-  // units per sequence and their prefix sums (every CTA computes them)
+  // clamped lengths, units per sequence and their prefix sums (every CTA)
   {
     const int nthr = PS::kThreads;
     const int per = (B + nthr - 1) / nthr;
@@ -336,26 +149,26 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     int local = 0;
     for (int b = lo; b < hi; ++b) {
       int L = p.context_lens[b];
-      L = L < 0 ? 0 : (L > l_max ? l_max : L);
+      if (L < 0 || L > l_max) {
+        if (blockIdx.x == 0) atomicOr(p.err, kErrLen);
+        L = L < 0 ? 0 : l_max;
+      }
+      lens[b] = L;
       local += (L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens) * Z;
     }
-    // exclusive scan of the per-thread sums (one warp, serially over warps' totals)
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int v = __shfl_up_sync(kFullMask, incl, off);
       if (lane >= off) incl += v;
     }
-    int* wsum = reinterpret_cast<int*>(meta);  // scratch before meta is used
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-    int woff = 0;
-    for (int w = 0; w < warp; ++w) woff += wsum[w];
-    int run = woff + incl - local;
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
     for (int b = lo; b < hi; ++b) {
       prefix[b] = run;
-      int L = p.context_lens[b];
-      L = L < 0 ? 0 : (L > l_max ? l_max : L);
+      const int L = lens[b];
       run += (L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens) * Z;
     }
     if (threadIdx.x == PS::kThreads - 1) {
@@ -368,6 +181,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         mbar_init(smem_u32(full + s), 1);
         mbar_init(smem_u32(empty + s), W);
       }
+      mbar_init(smem_u32(cbar), W);
       fence_mbar_init();
     }
     __syncthreads();
@@ -382,113 +196,160 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     }
     int* sched_next = p.err + kSchedNextOffset;
     int* sched_done = p.err + kSchedDoneOffset;
-    int k = 0;
-    bool ok = true;
-    auto acquire_stage = [&](int kk) -> bool {
-      const int s = kk % S;
-      bool got = true;
-      if (lane == 0) got = mbar_wait_bounded(smem_u32(empty + s), ((kk / S) & 1) ^ 1, p.wait_limit_ns);
-      return __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
-    };
-    while (ok) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(sched_next, 1);
-      u = __shfl_sync(kFullMask, u, 0);
-      if (u >= total_units) break;
-      // sequence of unit u: prefix[b] <= u < prefix[b+1]
+
+    auto decode_unit = [&](int u) {
+      UnitInfo x;
       int lo = 0, hi = B - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (prefix[mid] <= u) lo = mid;
         else hi = mid - 1;
       }
-      const int b = lo;
-      const int r = u - prefix[b];
-      const int part = r / Z, z = r - (r / Z) * Z;
-      int L = p.context_lens[b];
-      if (L < 0 || L > l_max) {
-        if (lane == 0 && part == 0 && z == 0) atomicOr(p.err, kErrLen);
-        L = L < 0 ? 0 : l_max;
+      x.b = lo;
+      const int r = u - prefix[lo];
+      x.part = r / Z;
+      x.z = r - x.part * Z;
+      const int L = lens[lo];
+      x.n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+      x.kvh = x.z / p.num_head_tiles;
+      x.h0 = x.kvh * p.group + (x.z - x.kvh * p.num_head_tiles) * HT;
+      x.nh = min(HT, p.group - (x.z - x.kvh * p.num_head_tiles) * HT);
+      x.tb = x.part * p.part_tokens;
+      x.te = min(L, x.tb + p.part_tokens);
+      x.n_chunks = L == 0 ? 0 : (x.te - x.tb + kChunk - 1) / kChunk;
+      return x;
+    };
+    // block-table entries of 16-token chunks cbase + lane (two when blocks hold 8 tokens)
+    auto load_entries = [&](const UnitInfo& x, int cbase, int& e0, int& e1) {
+      e0 = 0;
+      e1 = 0;
+      const int cc = cbase + lane;
+      if (cc < x.n_chunks) {
+        const int32_t* bt_row = p.block_tables + static_cast<int64_t>(x.b) * p.bt_stride;
+        const int t0 = x.tb + kChunk * cc;
+        int x0 = bt_row[t0 >> p.log2_bs], x1 = 0;
+        if (p.log2_bs < 4 && t0 + 8 < x.te) x1 = bt_row[(t0 >> p.log2_bs) + 1];
+        if (x0 < 0 || x0 >= p.num_blocks || x1 < 0 || x1 >= p.num_blocks) {
+          atomicOr(p.err, kErrBlock);
+          x0 = (x0 < 0 || x0 >= p.num_blocks) ? 0 : x0;
+          x1 = (x1 < 0 || x1 >= p.num_blocks) ? 0 : x1;
+        }
+        e0 = x0;
+        e1 = x1;
       }
-      const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-      const int kvh = z / p.num_head_tiles, ht = z - kvh * p.num_head_tiles;
-      const int h0 = kvh * p.group + ht * HT;
-      const int nh = min(HT, p.group - ht * HT);
-      const int tb = part * p.part_tokens;
-      const int te = min(L, tb + p.part_tokens);
-      const int n_chunks = L == 0 ? 0 : (te - tb + kChunk - 1) / kChunk;
-      if (n_chunks == 0) {
+    };
+    int k = 0;  // stage sequence number
+    bool ok = true;
+    auto acquire_stage = [&](int kk) -> bool {
+      bool got = true;
+      if (lane == 0) got = mbar_wait_bounded(smem_u32(empty + kk % S), ((kk / S) & 1) ^ 1, p.wait_limit_ns);
+      return __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+    };
+
+    // the unit being issued, the next one (entries prefetched), and the id
+    // after that (its atomic still in flight)
+    // the first unit of CTA i is unit i; later ones come from the counter
+    // (offset by the grid size)
+    int u_cur = static_cast<int>(blockIdx.x);
+    UnitInfo cur{};
+    int e0 = 0, e1 = 0;
+    if (u_cur < total_units) {
+      cur = decode_unit(u_cur);
+      load_entries(cur, 0, e0, e1);
+    }
+    int raw_next = 0;
+    if (lane == 0 && u_cur < total_units) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+    while (ok && u_cur < total_units) {
+      const int u_nxt = u_cur < total_units ? __shfl_sync(kFullMask, raw_next, 0) : total_units;
+      UnitInfo nxt{};
+      int f0 = 0, f1 = 0;
+      if (u_nxt < total_units) {
+        nxt = decode_unit(u_nxt);
+        load_entries(nxt, 0, f0, f1);
+        if (lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+      }
+      // issue the current unit
+      if (cur.n_chunks == 0) {
         if (!acquire_stage(k)) { ok = false; break; }
         if (lane == 0) {
-          meta[k % S] = ChunkMeta{b, part, 0, 0, n_parts, h0, nh, kFirst | kLast | kEmptySeq, z, 0, 0, 0};
+          meta[k % S] = StageMeta{cur.b, cur.part, 0, 0, cur.n_parts, cur.h0, cur.nh,
+                                  kFirst | kLast | kEmptySeq, cur.z, 0, 0, 0};
           mbar_arrive_expect_tx(smem_u32(full + k % S), 0);
         }
         ++k;
-        continue;
-      }
-      const int32_t* bt_row = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
-      const T* qsrc = reinterpret_cast<const T*>(p.q) + b * p.q_sb + static_cast<int64_t>(h0) * p.q_sh;
-      int e0 = 0, e1 = 0;
-      for (int c = 0; c < n_chunks; ++c) {
-        if ((c & 31) == 0) {  // this unit's next 32 table entries, one per lane
-          const int cc = c + lane;
-          e0 = 0;
-          e1 = 0;
-          if (cc < n_chunks) {
-            const int t0 = tb + kChunk * cc;
-            int x0 = bt_row[t0 >> p.log2_bs], x1 = 0;
-            if (p.log2_bs < 4 && t0 + 8 < te) x1 = bt_row[(t0 >> p.log2_bs) + 1];
-            if (x0 < 0 || x0 >= p.num_blocks || x1 < 0 || x1 >= p.num_blocks) {
-              atomicOr(p.err, kErrBlock);
-              x0 = (x0 < 0 || x0 >= p.num_blocks) ? 0 : x0;
-              x1 = (x1 < 0 || x1 >= p.num_blocks) ? 0 : x1;
-            }
-            e0 = x0;
-            e1 = x1;
+      } else {
+        const T* qsrc = reinterpret_cast<const T*>(p.q) + cur.b * p.q_sb + static_cast<int64_t>(cur.h0) * p.q_sh;
+        const int n_stages = (cur.n_chunks + kSub - 1) / kSub;
+        for (int sg = 0; sg < n_stages; ++sg) {
+          const int c0 = sg * kSub;
+          if (c0 > 0 && (c0 & 31) == 0) load_entries(cur, c0, e0, e1);
+          int pbs0[kSub], pbs1[kSub];
+#pragma unroll
+          for (int j = 0; j < kSub; ++j) {
+            pbs0[j] = __shfl_sync(kFullMask, e0, (c0 + j) & 31);
+            pbs1[j] = __shfl_sync(kFullMask, e1, (c0 + j) & 31);
           }
-        }
-        const int pb0 = __shfl_sync(kFullMask, e0, c & 31);
-        const int pb1 = __shfl_sync(kFullMask, e1, c & 31);
-        if (!acquire_stage(k)) { ok = false; break; }
-        if (lane == 0) {
-          const int s = k % S;
-          const int t0 = tb + kChunk * c;
-          const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
-          const uint32_t bar = smem_u32(full + s);
-          const int flags = (c == 0 ? kFirst : 0) | (c == n_chunks - 1 ? kLast : 0);
-          meta[s] = ChunkMeta{b, part, t0, te, n_parts, h0, nh, flags, z, 0, 0, 0};
-          const bool two = p.log2_bs < 4;
-          const bool has1 = two && (t0 + 8 < te);
-          uint32_t bytes = (two && !has1) ? G::kStageBytes / 2 : G::kStageBytes;
-          if (c == 0) bytes += nh * D * static_cast<int>(sizeof(T));
-          mbar_arrive_expect_tx(bar, bytes);
-          if (!two) {
-            const int y = kvh * p.block_size + (t0 & (p.block_size - 1));
+          if (!acquire_stage(k)) { ok = false; break; }
+          if (lane == 0) {
+            const int s = k % S;
+            const int t0 = cur.tb + kChunk * c0;
+            const int nsub = min(kSub, cur.n_chunks - c0);
+            const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
+            const uint32_t bar = smem_u32(full + s);
+            const int flags = (sg == 0 ? kFirst : 0) | (sg == n_stages - 1 ? kLast : 0);
+            meta[s] = StageMeta{cur.b, cur.part, t0, cur.te, cur.n_parts, cur.h0, cur.nh, flags, cur.z, nsub, 0, 0};
+            const bool two = p.log2_bs < 4;
+            uint32_t bytes = 0;
 #pragma unroll
-            for (int cb = 0; cb < G::kColBoxes; ++cb) {
-              tma_load_3d(stage + cb * 2048, &kmap, bar, cb * G::kBoxCols, y, pb0);
-              tma_load_3d(stage + PS::kKV + cb * 2048, &vmap, bar, cb * G::kBoxCols, y, pb0);
-            }
-          } else {
-            const int y = kvh * p.block_size;
-#pragma unroll
-            for (int cb = 0; cb < G::kColBoxes; ++cb) {
-              tma_load_3d(stage + cb * 2048, &kmap, bar, cb * G::kBoxCols, y, pb0);
-              tma_load_3d(stage + PS::kKV + cb * 2048, &vmap, bar, cb * G::kBoxCols, y, pb0);
-              if (has1) {
-                tma_load_3d(stage + cb * 2048 + 1024, &kmap, bar, cb * G::kBoxCols, y, pb1);
-                tma_load_3d(stage + PS::kKV + cb * 2048 + 1024, &vmap, bar, cb * G::kBoxCols, y, pb1);
+            for (int j = 0; j < kSub; ++j) {
+              if (j < nsub) {
+                const int tj = t0 + kChunk * j;
+                bytes += (two && !(tj + 8 < cur.te)) ? G::kStageBytes / 2 : G::kStageBytes;
               }
             }
+            if (sg == 0) bytes += cur.nh * D * static_cast<int>(sizeof(T));
+            mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) {
+              if (j < nsub) {
+                const int tj = t0 + kChunk * j;
+                const uint32_t kdst = stage + j * PS::kKV;
+                const uint32_t vdst = stage + (kSub + j) * PS::kKV;
+                if (!two) {
+                  const int y = cur.kvh * p.block_size + (tj & (p.block_size - 1));
+#pragma unroll
+                  for (int cb = 0; cb < G::kColBoxes; ++cb) {
+                    tma_load_3d(kdst + cb * 2048, &kmap, bar, cb * G::kBoxCols, y, pbs0[j]);
+                    tma_load_3d(vdst + cb * 2048, &vmap, bar, cb * G::kBoxCols, y, pbs0[j]);
+                  }
+                } else {
+                  const int y = cur.kvh * p.block_size;
+                  const bool has1 = tj + 8 < cur.te;
+#pragma unroll
+                  for (int cb = 0; cb < G::kColBoxes; ++cb) {
+                    tma_load_3d(kdst + cb * 2048, &kmap, bar, cb * G::kBoxCols, y, pbs0[j]);
+                    tma_load_3d(vdst + cb * 2048, &vmap, bar, cb * G::kBoxCols, y, pbs0[j]);
+                    if (has1) {
+                      tma_load_3d(kdst + cb * 2048 + 1024, &kmap, bar, cb * G::kBoxCols, y, pbs1[j]);
+                      tma_load_3d(vdst + cb * 2048 + 1024, &vmap, bar, cb * G::kBoxCols, y, pbs1[j]);
+                    }
+                  }
+                }
+              }
+            }
+            if (sg == 0) {
+              for (int hh = 0; hh < cur.nh; ++hh)
+                bulk_load(stage + 2 * kSub * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
+                          D * static_cast<int>(sizeof(T)), bar);
+            }
           }
-          if (c == 0) {
-            for (int hh = 0; hh < nh; ++hh)
-              bulk_load(stage + 2 * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
-                        D * static_cast<int>(sizeof(T)), bar);
-          }
+          ++k;
         }
-        ++k;
       }
+      cur = nxt;
+      e0 = f0;
+      e1 = f1;
+      u_cur = u_nxt;
     }
     // tell the consumers to stop, then leave the scheduler clean
     if (ok && acquire_stage(k)) {
@@ -510,90 +371,194 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   }
 
   // ------------------------------- consumers --------------------------------
-  PState<T, D, NT> st;
+  MmaState<T, D, NT> st;
   const int cw = warp;
+  float* red_o = reinterpret_cast<float*>(red_area);  // [W][HT][D]
+  float* red_m = red_o + W * HT * D;                  // [W][HT]
+  float* red_l = red_m + W * HT;                      // [W][HT]
+  const uint32_t sync_bar = smem_u32(cbar);
+  int sync_phase = 0;
+  T* out = reinterpret_cast<T*>(p.out);
   for (int k = 0;; ++k) {
     const int s = k % S;
     if (!mbar_wait_bounded(smem_u32(full + s), (k / S) & 1, p.wait_limit_ns)) {
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
       return;
     }
-    const ChunkMeta mt_ = meta[s];
+    const StageMeta mt_ = meta[s];
     if (mt_.flags & kStop) return;
     const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
     if (!(mt_.flags & kEmptySeq)) {
-      if (mt_.flags & kFirst) pstate_begin<T, D, NT>(st, ring + s * PS::kStageBytes + 2 * PS::kKV, mt_.nh, lane);
-      pstate_chunk<T, D, NT>(st, stage, stage + PS::kKV, mt_.t0, mt_.tok_end, p.scale_log2, cw, lane);
+      if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, ring + s * PS::kStageBytes + 2 * kSub * PS::kKV, mt_.nh, lane);
+      if (cw < mt_.nsub)
+        mma_chunk<T, D, NT>(st, stage + cw * PS::kKV, stage + (kSub + cw) * PS::kKV, mt_.t0 + cw * kChunk,
+                            mt_.tok_end, p.scale_log2, lane);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(empty + s));
-    if (mt_.flags & kLast) pstate_finish<T, D, NT>(st, mt_, p, cw, lane);
+    if (!(mt_.flags & kLast)) continue;
+
+    // ---- the unit is complete: merge the four warps, write out or a partial
+    const int b = mt_.b, h0 = mt_.h0, nh = mt_.nh;
+    if (mt_.flags & kEmptySeq) {
+      for (int idx = cw * 32 + lane; idx < nh * D; idx += W * 32) {
+        const int hh = idx / D, d = idx - (idx / D) * D;
+        out[b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh + d] = from_f32<T>(0.f);
+      }
+      continue;
+    }
+    mma_store<T, D, NT>(st, red_o + cw * HT * D, red_m + cw * HT, red_l + cw * HT, lane);
+    if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
+      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+      return;
+    }
+    const bool split = mt_.n_parts > 1;
+    const int row0 = b * p.num_q_heads + h0;
+    for (int hh = cw; hh < nh; hh += W) {
+      float mw[W], M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        mw[w] = red_m[w * HT + hh];
+        M = fmaxf(M, mw[w]);
+      }
+      float fw[W], den = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        fw[w] = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
+        den += fw[w] * red_l[w * HT + hh];
+      }
+      if (!split) {
+        const float inv = 1.f / den;
+        T* orow = out + b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          const int d = lane + 32 * i;
+          float num = 0.f;
+#pragma unroll
+          for (int w = 0; w < W; ++w) num += fw[w] * red_o[(w * HT + hh) * D + d];
+          orow[d] = from_f32<T>(num * inv);
+        }
+      } else {
+        const int64_t slot = static_cast<int64_t>(row0 + hh) * p.max_parts + mt_.p;
+        float* wo = p.ws_o + slot * D;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          const int d = lane + 32 * i;
+          float num = 0.f;
+#pragma unroll
+          for (int w = 0; w < W; ++w) num += fw[w] * red_o[(w * HT + hh) * D + d];
+          wo[d] = num;
+        }
+        if (lane == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, den);
+      }
+    }
+    if (split && p.ws_count != nullptr) __threadfence();
+    if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {  // reduction area free again
+      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+      return;
+    }
+    if (!split || p.ws_count == nullptr || D > 128) continue;
+
+    // few partitions: the last CTA to finish one of (b, z) combines them all
+    int* counter = p.ws_count + static_cast<int64_t>(b) * p.num_kv_heads * p.num_head_tiles + mt_.z;
+    if (cw == 0 && lane == 0) last_flag[0] = atomicAdd(counter, 1) == mt_.n_parts - 1;
+    if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
+      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+      return;
+    }
+    // (the flag is rewritten only after the next unit's first rendezvous,
+    // which every warp reaches after reading it here)
+    const int last = last_flag[0];
+    if (!last) continue;
+    __threadfence();
+    const int n_parts = mt_.n_parts;
+    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml);
+    for (int hh = cw; hh < nh; hh += W) {
+      const int64_t base = static_cast<int64_t>(row0 + hh) * p.max_parts;
+      // every load first (one round trip), then the arithmetic
+      float2 v[kInKernelCombineMaxParts];
+      float o[kInKernelCombineMaxParts][D / 32];
+#pragma unroll
+      for (int pp = 0; pp < kInKernelCombineMaxParts; ++pp) {
+        if (pp < n_parts) {
+          v[pp] = __ldcg(ml + base + pp);
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) o[pp][i] = __ldcg(p.ws_o + (base + pp) * D + lane + 32 * i);
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int pp = 0; pp < kInKernelCombineMaxParts; ++pp)
+        if (pp < n_parts) M = fmaxf(M, v[pp].x);
+      float den = 0.f, num[D / 32];
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < kInKernelCombineMaxParts; ++pp) {
+        if (pp < n_parts) {
+          const float f = exp2f(v[pp].x - M);
+          den = fmaf(f, v[pp].y, den);
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) num[i] = fmaf(f, o[pp][i], num[i]);
+        }
+      }
+      const float inv = 1.f / den;
+      T* orow = out + b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
+    }
+    if (cw == 0 && lane == 0) *counter = 0;
   }
 }
 
-// Combine kernel for launches with many partitions per sequence: one CTA per
-// query row (b, h); warps split the partitions, lanes the columns.
+// Combine kernel for launches with many partitions per sequence: one warp per
+// query row (b, h); lanes hold the partitions' weights and the output columns.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p, int ml_stride) {
-  const int row = blockIdx.x;
+__global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= p.num_seqs * p.num_q_heads) return;
   const int b = row / p.num_q_heads;
   int L = p.context_lens[b];
   const int l_max = p.max_blocks * p.block_size;
   L = L < 0 ? 0 : (L > l_max ? l_max : L);
   const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
   if (n_parts == 1) return;  // written by the decode kernel
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kWarps = 8;
-  constexpr int kPer = D / 32;  // columns per lane
-  __shared__ float red_m[kWarps];
-  __shared__ float red_l[kWarps];
-  __shared__ float red_o[kWarps][D];
   const int64_t base = static_cast<int64_t>(row) * p.max_parts;
   const float2* ml = reinterpret_cast<const float2*>(p.ws_ml);
   float M = -INFINITY;
-  for (int pp = threadIdx.x; pp < n_parts; pp += blockDim.x) M = fmaxf(M, ml[(base + pp) * ml_stride].x);
+  for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, ml[base + pp].x);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
-  if (lane == 0) red_m[warp] = M;
-  __syncthreads();
-  M = red_m[0];
+  float den = 0.f, num[D / 32];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red_m[w]);
-  float den = 0.f, num[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) num[i] = 0.f;
-  for (int pp = warp; pp < n_parts; pp += kWarps) {
-    const float2 v = ml[(base + pp) * ml_stride];
-    const float f = exp2f(v.x - M);
+  for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
+  for (int p0 = 0; p0 < n_parts; p0 += 32) {
+    const bool mine = p0 + lane < n_parts;
+    const float2 v = mine ? ml[base + p0 + lane] : make_float2(-INFINITY, 0.f);
+    const float f = mine ? exp2f(v.x - M) : 0.f;
     den += f * v.y;
-    const float* o = p.ws_o + (base + pp) * D;
+    const int cnt = min(32, n_parts - p0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float fp = __shfl_sync(kFullMask, f, j);
+      const float* o = p.ws_o + (base + p0 + j) * D;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) num[i] = fmaf(f, o[lane + 32 * i], num[i]);
-  }
-  if (lane == 0) red_l[warp] = den;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) red_o[warp][lane + 32 * i] = num[i];
-  __syncthreads();
-  if (warp == 0) {
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += red_l[w];
-    const float inv = 1.f / tot;
-    const int h = row - b * p.num_q_heads;
-    T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      float acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) acc += red_o[w][lane + 32 * i];
-      orow[lane + 32 * i] = from_f32<T>(acc * inv);
+      for (int i = 0; i < D / 32; ++i) num[i] = fmaf(fp, o[lane + 32 * i], num[i]);
     }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
+  const float inv = 1.f / den;
+  const int h = row - b * p.num_q_heads;
+  T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
 }
 
 template <typename T, int D, int NT>
 int persistent_smem(int num_seqs) {
-  return PShape<T, D, NT>::kFixedSmem + ((num_seqs + 1) * 4 + 15) / 16 * 16;
+  return PShape<T, D, NT>::kFixedSmem + ((2 * num_seqs + 1) * 4 + 15) / 16 * 16;
 }
 
 template <typename T, int D, int NT>
@@ -614,7 +579,7 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
   kernel<<<grid, PS::kThreads, smem, stream>>>(kmap, vmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || !separate_combine) return e;
-  splitkv_combine<T, D><<<p.num_seqs * p.num_q_heads, 256, 0, stream>>>(p, PS::kConsumers);
+  splitkv_combine<T, D><<<(p.num_seqs * p.num_q_heads + 7) / 8, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -622,6 +587,9 @@ template <typename T, int D, int NT>
 int persistent_occupancy(int num_seqs) {
   int blocks = 0;
   const int smem = persistent_smem<T, D, NT>(num_seqs);
+  if (cudaFuncSetAttribute(paged_decode_persistent<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           227 * 1024) != cudaSuccess)
+    return 1;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_persistent<T, D, NT>,
                                                     PShape<T, D, NT>::kThreads, smem) != cudaSuccess)
     return 1;

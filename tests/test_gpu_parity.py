@@ -360,7 +360,7 @@ def test_unaligned_query_rows_fall_back():
 
 
 def test_large_batch_is_sliced():
-    """More sequences than one persistent launch takes (4096)."""
+    """More sequences than one persistent launch takes (1024): the host slices the batch."""
     g = torch.Generator().manual_seed(13)
     lens = torch.randint(1, 40, (4300,), generator=g).tolist()
     case = workloads.custom_case("big", lens=lens, num_q_heads=4, num_kv_heads=1, head_dim=64,

@@ -340,9 +340,8 @@ DecodePlan make_plan(int dt, int64_t B, int64_t hq, int64_t hkv, int64_t d, int6
     pl.part_tokens = choose_partition_persistent(B, z, tokens_max, n_ctas);
     pl.max_parts = static_cast<int>((tokens_max + pl.part_tokens - 1) / pl.part_tokens);
     pl.grid = static_cast<int>(std::min<int64_t>(n_ctas, std::max<int64_t>(1, B * z * pl.max_parts)));
-    pl.separate_combine = pl.max_parts > kInKernelCombineMaxParts || d > 128;
+    pl.separate_combine = pl.max_parts > 1;
     if (pl.max_parts > 1) {
-      pl.counter_bytes = pl.separate_combine ? 0 : align256(size_t(B) * z * sizeof(int));
       pl.ml_bytes = align256(size_t(B) * hq * pl.max_parts * 2 * sizeof(float));
       pl.o_bytes = align256(size_t(B) * hq * pl.max_parts * d * sizeof(float));
     }

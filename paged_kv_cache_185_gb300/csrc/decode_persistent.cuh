@@ -21,9 +21,13 @@
 // At the end of a unit the consumers merge their four (m, l, O) through
 // shared memory (two rendezvous on a bounded mbarrier).  A sequence with one
 // partition gets its output written there; otherwise the merged partial goes
-// to the workspace and, with few partitions, the last CTA to arrive for
-// (b, z) -- an atomic counter, never waited for -- combines them; with many, a
-// separate combine kernel does it after the launch.
+// to the workspace and a combine kernel, launched right after, merges the
+// partitions (so no consumer ever waits on a fence or an atomic).
+//
+// Unit order: first every (sequence, kv-head tile) at partition 0 -- CTA i
+// starts on unit i at once, needing only sequence i / Z's length and table
+// row, while the consumer warps build the prefix sums that map the later
+// units (partitions >= 1, sequence-major) -- then the rest from the counter.
 //
 // Every wait is bounded: on timeout the warp records an error bit and leaves.
 // The scheduler counter is reset by the last CTA to finish, so it is zero
@@ -68,7 +72,7 @@ struct PShape {
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kBarBytes = (2 * kStages + 1) * 8;
+  static constexpr int kBarBytes = (2 * kStages + 2) * 8;
   static constexpr int kMetaBytes = kStages * static_cast<int>(sizeof(StageMeta));
   static constexpr int kFixedSmem = 1024 + kRingBytes + kRedBytes + kBarBytes + kMetaBytes + 64;
 };
@@ -130,9 +134,9 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   uint64_t* full = reinterpret_cast<uint64_t*>(red_area + PS::kRedBytes);
   uint64_t* empty = full + S;
   uint64_t* cbar = empty + S;                 // consumer rendezvous
-  StageMeta* meta = reinterpret_cast<StageMeta*>(cbar + 1);
+  uint64_t* pbar = cbar + 1;                  // prefix sums ready (consumers -> producer)
+  StageMeta* meta = reinterpret_cast<StageMeta*>(pbar + 1);
   int* wsum = reinterpret_cast<int*>(meta + S);  // 16 ints of scratch
-  int* last_flag = wsum;                         // reused once the prefix sums are done
   int* prefix = wsum + 16;                       // [B + 1] units before sequence b
   int* lens = prefix + p.num_seqs + 1;           // [B] clamped context lengths
 
@@ -141,52 +145,17 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   const int Z = p.num_kv_heads * p.num_head_tiles;
   const int l_max = p.max_blocks * p.block_size;
 
-  // clamped lengths, units per sequence and their prefix sums (every CTA)
-  {
-    const int nthr = PS::kThreads;
-    const int per = (B + nthr - 1) / nthr;
-    const int lo = threadIdx.x * per, hi = min(B, lo + per);
-    int local = 0;
-    for (int b = lo; b < hi; ++b) {
-      int L = p.context_lens[b];
-      if (L < 0 || L > l_max) {
-        if (blockIdx.x == 0) atomicOr(p.err, kErrLen);
-        L = L < 0 ? 0 : l_max;
-      }
-      lens[b] = L;
-      local += (L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens) * Z;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), W);
     }
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int run = incl - local;
-    for (int w = 0; w < warp; ++w) run += wsum[w];
-    for (int b = lo; b < hi; ++b) {
-      prefix[b] = run;
-      const int L = lens[b];
-      run += (L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens) * Z;
-    }
-    if (threadIdx.x == PS::kThreads - 1) {
-      int tot = 0;
-      for (int w = 0; w < PS::kThreads / 32; ++w) tot += wsum[w];
-      prefix[B] = tot;
-    }
-    if (threadIdx.x == 0) {
-      for (int s = 0; s < S; ++s) {
-        mbar_init(smem_u32(full + s), 1);
-        mbar_init(smem_u32(empty + s), W);
-      }
-      mbar_init(smem_u32(cbar), W);
-      fence_mbar_init();
-    }
-    __syncthreads();
+    mbar_init(smem_u32(cbar), W);
+    mbar_init(smem_u32(pbar), 1);
+    fence_mbar_init();
   }
-  const int total_units = prefix[B];
+  __syncthreads();
+  const int BZ = B * Z;  // partition-0 units
 
   if (warp == W) {
     // ------------------------------- producer -------------------------------
@@ -197,28 +166,6 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     int* sched_next = p.err + kSchedNextOffset;
     int* sched_done = p.err + kSchedDoneOffset;
 
-    auto decode_unit = [&](int u) {
-      UnitInfo x;
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= u) lo = mid;
-        else hi = mid - 1;
-      }
-      x.b = lo;
-      const int r = u - prefix[lo];
-      x.part = r / Z;
-      x.z = r - x.part * Z;
-      const int L = lens[lo];
-      x.n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-      x.kvh = x.z / p.num_head_tiles;
-      x.h0 = x.kvh * p.group + (x.z - x.kvh * p.num_head_tiles) * HT;
-      x.nh = min(HT, p.group - (x.z - x.kvh * p.num_head_tiles) * HT);
-      x.tb = x.part * p.part_tokens;
-      x.te = min(L, x.tb + p.part_tokens);
-      x.n_chunks = L == 0 ? 0 : (x.te - x.tb + kChunk - 1) / kChunk;
-      return x;
-    };
     // block-table entries of 16-token chunks cbase + lane (two when blocks hold 8 tokens)
     auto load_entries = [&](const UnitInfo& x, int cbase, int& e0, int& e1) {
       e0 = 0;
@@ -238,6 +185,69 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         e1 = x1;
       }
     };
+    bool have_prefix = false;
+    bool wait_ok = true;
+    // unit u -> (sequence, partition, kv-head tile) and the table entries of
+    // its first 32 chunks (two per chunk when blocks hold 8 tokens).  Returns
+    // false past the last unit.
+    auto decode_unit = [&](int u, UnitInfo& x, int& e0, int& e1) -> bool {
+      int L;
+      if (u < BZ) {
+        x.b = u / Z;
+        x.z = u - x.b * Z;
+        x.part = 0;
+        int Lraw = p.context_lens[x.b];  // issued together with the table loads below
+        const int32_t* bt_row = p.block_tables + static_cast<int64_t>(x.b) * p.bt_stride;
+        const int j0 = (kChunk * lane) >> p.log2_bs;
+        int r0 = j0 < p.max_blocks ? bt_row[j0] : 0;
+        int r1 = (p.log2_bs < 4 && j0 + 1 < p.max_blocks) ? bt_row[j0 + 1] : 0;
+        if (Lraw < 0 || Lraw > l_max) {
+          if (lane == 0) atomicOr(p.err, kErrLen);
+          Lraw = Lraw < 0 ? 0 : l_max;
+        }
+        L = Lraw;
+        x.tb = 0;
+        x.te = min(L, p.part_tokens);
+        x.n_chunks = L == 0 ? 0 : (x.te + kChunk - 1) / kChunk;
+        const int t0 = kChunk * lane;
+        const bool need0 = lane < x.n_chunks, need1 = need0 && p.log2_bs < 4 && t0 + 8 < x.te;
+        if ((need0 && (r0 < 0 || r0 >= p.num_blocks)) || (need1 && (r1 < 0 || r1 >= p.num_blocks))) {
+          atomicOr(p.err, kErrBlock);
+        }
+        e0 = (need0 && r0 >= 0 && r0 < p.num_blocks) ? r0 : 0;
+        e1 = (need1 && r1 >= 0 && r1 < p.num_blocks) ? r1 : 0;
+      } else {
+        if (!have_prefix) {
+          bool got = true;
+          if (lane == 0) got = mbar_wait_bounded(smem_u32(pbar), 0, p.wait_limit_ns);
+          wait_ok = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+          have_prefix = true;
+          if (!wait_ok) return false;
+        }
+        const int u2 = u - BZ;
+        if (u2 >= prefix[B]) return false;
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= u2) lo = mid;
+          else hi = mid - 1;
+        }
+        x.b = lo;
+        const int r = u2 - prefix[lo];
+        x.part = 1 + r / Z;
+        x.z = r - (r / Z) * Z;
+        L = lens[lo];
+        x.tb = x.part * p.part_tokens;
+        x.te = min(L, x.tb + p.part_tokens);
+        x.n_chunks = (x.te - x.tb + kChunk - 1) / kChunk;
+        load_entries(x, 0, e0, e1);
+      }
+      x.n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+      x.kvh = x.z / p.num_head_tiles;
+      x.h0 = x.kvh * p.group + (x.z - x.kvh * p.num_head_tiles) * HT;
+      x.nh = min(HT, p.group - (x.z - x.kvh * p.num_head_tiles) * HT);
+      return true;
+    };
     int k = 0;  // stage sequence number
     bool ok = true;
     auto acquire_stage = [&](int kk) -> bool {
@@ -249,26 +259,25 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     // the unit being issued, the next one (entries prefetched), and the id
     // after that (its atomic still in flight)
     // the first unit of CTA i is unit i; later ones come from the counter
-    // (offset by the grid size)
-    int u_cur = static_cast<int>(blockIdx.x);
+    // (offset by the grid size); the next id is always requested one unit
+    // ahead so its latency hides behind the current unit's copies
     UnitInfo cur{};
     int e0 = 0, e1 = 0;
-    if (u_cur < total_units) {
-      cur = decode_unit(u_cur);
-      load_entries(cur, 0, e0, e1);
-    }
+    bool have_cur = decode_unit(static_cast<int>(blockIdx.x), cur, e0, e1);
     int raw_next = 0;
-    if (lane == 0 && u_cur < total_units) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
-    while (ok && u_cur < total_units) {
-      const int u_nxt = u_cur < total_units ? __shfl_sync(kFullMask, raw_next, 0) : total_units;
+    if (lane == 0 && have_cur) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+    while (ok && have_cur) {
+      // the next unit is fetched once the current one has filled the ring
+      // (or has no more stages), so its latency overlaps the copies in flight
       UnitInfo nxt{};
       int f0 = 0, f1 = 0;
-      if (u_nxt < total_units) {
-        nxt = decode_unit(u_nxt);
-        load_entries(nxt, 0, f0, f1);
-        if (lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
-      }
-      // issue the current unit
+      bool have_nxt = false, fetched = false;
+      auto fetch_next = [&]() {
+        const int u_nxt = __shfl_sync(kFullMask, raw_next, 0);
+        have_nxt = decode_unit(u_nxt, nxt, f0, f1);
+        if (have_nxt && lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+        fetched = true;
+      };
       if (cur.n_chunks == 0) {
         if (!acquire_stage(k)) { ok = false; break; }
         if (lane == 0) {
@@ -280,6 +289,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
       } else {
         const T* qsrc = reinterpret_cast<const T*>(p.q) + cur.b * p.q_sb + static_cast<int64_t>(cur.h0) * p.q_sh;
         const int n_stages = (cur.n_chunks + kSub - 1) / kSub;
+        const int fetch_after = (n_stages < S ? n_stages : S) - 1;
         for (int sg = 0; sg < n_stages; ++sg) {
           const int c0 = sg * kSub;
           if (c0 > 0 && (c0 & 31) == 0) load_entries(cur, c0, e0, e1);
@@ -344,14 +354,20 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
             }
           }
           ++k;
+          if (sg == fetch_after) fetch_next();
+          if (!wait_ok) { ok = false; break; }
         }
       }
+      if (!ok) break;
+      if (!fetched) fetch_next();
+      if (!wait_ok) { ok = false; break; }
       cur = nxt;
       e0 = f0;
       e1 = f1;
-      u_cur = u_nxt;
+      have_cur = have_nxt;
     }
     // tell the consumers to stop, then leave the scheduler clean
+    if (!wait_ok) ok = false;
     if (ok && acquire_stage(k)) {
       if (lane == 0) {
         meta[k % S].flags = kStop;
@@ -371,6 +387,38 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   }
 
   // ------------------------------- consumers --------------------------------
+  // prefix sums of the units at partitions >= 1, sequence-major, and the
+  // clamped lengths; then tell the producer
+  {
+    constexpr int kCT = W * 32;
+    const int per = (B + kCT - 1) / kCT;
+    const int lo = threadIdx.x * per, hi = min(B, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) {
+      int L = p.context_lens[b];
+      L = L < 0 ? 0 : (L > l_max ? l_max : L);
+      lens[b] = L;
+      local += (L == 0 ? 0 : (L + p.part_tokens - 1) / p.part_tokens - 1) * Z;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int b = lo; b < hi; ++b) {
+      prefix[b] = run;
+      const int L = lens[b];
+      run += (L == 0 ? 0 : (L + p.part_tokens - 1) / p.part_tokens - 1) * Z;
+    }
+    if (threadIdx.x == kCT - 1) prefix[B] = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+    asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
+    if (threadIdx.x == 0) mbar_arrive(smem_u32(pbar));
+  }
   MmaState<T, D, NT> st;
   const int cw = warp;
   float* red_o = reinterpret_cast<float*>(red_area);  // [W][HT][D]
@@ -452,66 +500,14 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         if (lane == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, den);
       }
     }
-    if (split && p.ws_count != nullptr) __threadfence();
     if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {  // reduction area free again
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
       return;
     }
-    if (!split || p.ws_count == nullptr || D > 128) continue;
-
-    // few partitions: the last CTA to finish one of (b, z) combines them all
-    int* counter = p.ws_count + static_cast<int64_t>(b) * p.num_kv_heads * p.num_head_tiles + mt_.z;
-    if (cw == 0 && lane == 0) last_flag[0] = atomicAdd(counter, 1) == mt_.n_parts - 1;
-    if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
-      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-      return;
-    }
-    // (the flag is rewritten only after the next unit's first rendezvous,
-    // which every warp reaches after reading it here)
-    const int last = last_flag[0];
-    if (!last) continue;
-    __threadfence();
-    const int n_parts = mt_.n_parts;
-    const float2* ml = reinterpret_cast<const float2*>(p.ws_ml);
-    for (int hh = cw; hh < nh; hh += W) {
-      const int64_t base = static_cast<int64_t>(row0 + hh) * p.max_parts;
-      // every load first (one round trip), then the arithmetic
-      float2 v[kInKernelCombineMaxParts];
-      float o[kInKernelCombineMaxParts][D / 32];
-#pragma unroll
-      for (int pp = 0; pp < kInKernelCombineMaxParts; ++pp) {
-        if (pp < n_parts) {
-          v[pp] = __ldcg(ml + base + pp);
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i) o[pp][i] = __ldcg(p.ws_o + (base + pp) * D + lane + 32 * i);
-        }
-      }
-      float M = -INFINITY;
-#pragma unroll
-      for (int pp = 0; pp < kInKernelCombineMaxParts; ++pp)
-        if (pp < n_parts) M = fmaxf(M, v[pp].x);
-      float den = 0.f, num[D / 32];
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
-#pragma unroll
-      for (int pp = 0; pp < kInKernelCombineMaxParts; ++pp) {
-        if (pp < n_parts) {
-          const float f = exp2f(v[pp].x - M);
-          den = fmaf(f, v[pp].y, den);
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i) num[i] = fmaf(f, o[pp][i], num[i]);
-        }
-      }
-      const float inv = 1.f / den;
-      T* orow = out + b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh;
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
-    }
-    if (cw == 0 && lane == 0) *counter = 0;
   }
 }
 
-// Combine kernel for launches with many partitions per sequence: one warp per
+// Combine kernel for launches that split sequences into partitions: one warp per
 // query row (b, h); lanes hold the partitions' weights and the output columns.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {

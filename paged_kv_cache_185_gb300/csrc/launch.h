@@ -57,15 +57,14 @@ int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& k
                   const CUtensorMap& vmap, const DecodeParams& p, cudaStream_t stream);
 
 // Persistent warp-specialised decode (f16/bf16 only).  `separate_combine`
-// appends the split-KV combine kernel; otherwise split partials are combined
-// in the decode kernel by the last CTA to finish a (sequence, kv-head tile).
+// appends the split-KV combine kernel (needed when a sequence can span
+// several partitions).
 int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
                              cudaStream_t stream);
 int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs);
 constexpr int kPersistentConsumers = 4;
 constexpr int kPersistentMaxSeqs = 1024;      // sequences per launch (the host splits larger batches)
-constexpr int kInKernelCombineMaxParts = 8;   // above this a separate combine kernel runs
 
 int launch_append(const AppendParams& p, cudaStream_t stream);
 

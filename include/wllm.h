@@ -144,6 +144,41 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q,
                                 float scale, int block_size, wllm_stream stream);
 
 /*
+ * Paged decode attention that allocates no device memory.
+ *
+ * There is no counterpart to this call in the pages; it exists for callers
+ * that cannot let a library allocate: one that is capturing a CUDA graph
+ * (cudaMalloc is not permitted inside a capture), an engine whose memory
+ * manager has already reserved all device memory for its own KV pool and
+ * activations, or a latency-critical caller that cannot accept the implicit
+ * device synchronisation of cudaMalloc/cudaFree.  It computes the same result
+ * with the same kernels as wllm_paged_attention_decode and takes the same
+ * arguments; the caller still owns and passes every input and output.
+ *
+ * Scratch: the split-KV partial results and the kernel's error and scheduler
+ * words live in one fixed 32 MiB array inside the library's device image,
+ * which every GPU that loads the library holds until the process exits.
+ *   - The first call on a device looks that array's device address up (once,
+ *     with the device current); make that first call before any stream
+ *     capture.
+ *   - Each call clears the words that must start at zero (a stream-ordered
+ *     memset of 256 bytes); the partials keep the last call's contents.
+ *   - All calls on a device share the array: calls that overlap on the GPU
+ *     (different streams, not ordered) race and give wrong results.
+ * Supported: F16/BF16 inputs, query rows 16-byte aligned (the persistent
+ * tensor-core kernel); anything else returns WLLM_ERR_UNSUPPORTED.  Sizes
+ * whose partial results would not fit in the array (many long sequences cut
+ * into many partitions) return WLLM_ERR_UNSUPPORTED with the byte counts in
+ * wllm_last_error(); nothing is launched then.  Check mode is not available
+ * here.
+ */
+int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tensor* q,
+                                        const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                                        const wllm_tensor* block_tables,
+                                        const wllm_tensor* context_lens, int num_kv_heads,
+                                        float scale, int block_size, wllm_stream stream);
+
+/*
  * Bytes of device workspace that wllm_paged_attention_decode needs for these
  * sizes (0 when no sequence is split).  The workspace holds the split-KV
  * partial results and one arrival counter per (sequence, kv head, head tile).

@@ -22,6 +22,7 @@ _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3,
 
 # every symbol include/wllm.h declares
 EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode",
+            "wllm_paged_attention_decode_noalloc",
             "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
             "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version")
 
@@ -62,6 +63,9 @@ def load_library():
         lib.wllm_paged_attention_decode.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
                                                     ctypes.c_int, ctypes.c_void_p]
         lib.wllm_paged_attention_decode.restype = ctypes.c_int
+        lib.wllm_paged_attention_decode_noalloc.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
+                                                            ctypes.c_int, ctypes.c_void_p]
+        lib.wllm_paged_attention_decode_noalloc.restype = ctypes.c_int
         lib.wllm_paged_attention_workspace_bytes.argtypes = [ctypes.c_int] * 6
         lib.wllm_paged_attention_workspace_bytes.restype = ctypes.c_size_t
         lib.wllm_set_workspace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
@@ -129,6 +133,19 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         args = [describe(x) for x in (out, q, k_cache, v_cache, block_tables, context_lens)]
         _check(lib.wllm_paged_attention_decode(*[ctypes.byref(a) for a in args], int(num_kv_heads),
                                                float(scale), int(block_size), _stream_handle(dev)))
+    return out
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   num_kv_heads: int, scale: float, block_size: int) -> torch.Tensor:
+    """Paged decode attention that allocates no device memory (fixed scratch
+    inside the library; see wllm_paged_attention_decode_noalloc in wllm.h)."""
+    dev = _require_cuda(out, q, k_cache, v_cache, block_tables, context_lens)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (out, q, k_cache, v_cache, block_tables, context_lens)]
+        _check(lib.wllm_paged_attention_decode_noalloc(*[ctypes.byref(a) for a in args], int(num_kv_heads),
+                                                       float(scale), int(block_size), _stream_handle(dev)))
     return out
 
 

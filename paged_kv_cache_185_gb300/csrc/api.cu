@@ -660,4 +660,168 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, co
   return WLLM_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// Some callers cannot let a library allocate device memory: a caller that is
+// capturing a CUDA graph (cudaMalloc is not allowed inside a capture), an
+// engine whose memory manager has reserved all device memory for its own KV
+// pool and activations, or a latency-critical caller that cannot accept the
+// implicit device synchronisation of cudaMalloc/cudaFree.  For them this
+// entry point takes its split-KV scratch (the per-partition partial results)
+// and its scheduler/error words from a fixed array in the library's device
+// image, sized kNoAllocScratchBytes.  Every GPU that loads the library holds
+// that array until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
+constexpr size_t kNoAllocControlBytes = 256;                // error + scheduler words
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+uint8_t* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device.  The host-side
+// symbol is only a stand-in; the real address comes from the runtime, once per
+// device, with that device current.
+int noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(WLLM_ERR_UNSUPPORTED, "device index %d too large", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_addr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  *out = g_noalloc_addr[dev];
+  return WLLM_OK;
+}
+
+}  // namespace
+
+int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                        const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                        const wllm_tensor* context_lens, int num_kv_heads, float scale,
+                                        int block_size, wllm_stream stream) {
+  int rc;
+  if ((rc = check_desc(out, "out", 3)) || (rc = check_desc(q, "q", 3)) ||
+      (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
+      (rc = check_desc(block_tables, "block_tables", 2)) || (rc = check_desc(context_lens, "context_lens", 1)))
+    return rc;
+  const int dt = q->dtype;
+  if (dt != WLLM_F16 && dt != WLLM_BF16)
+    return fail(WLLM_ERR_UNSUPPORTED, "the allocation-free decode takes F16 or BF16 inputs");
+  if (out->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
+    return fail(WLLM_ERR_INVALID_ARG, "q, out and caches must share one dtype");
+  if (block_tables->dtype != WLLM_I32) return fail(WLLM_ERR_INVALID_ARG, "block_tables: dtype must be I32");
+  if (context_lens->dtype != WLLM_I32) return fail(WLLM_ERR_INVALID_ARG, "context_lens: dtype must be I32");
+  if (!same_shape(out, q)) return fail(WLLM_ERR_INVALID_ARG, "out and q shapes differ");
+  if (!same_shape(k_cache, v_cache)) return fail(WLLM_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  const int64_t B = q->shape[0], hq = q->shape[1], d = q->shape[2];
+  const int64_t nb = k_cache->shape[0], hkv = k_cache->shape[1], bs = k_cache->shape[2];
+  if (k_cache->shape[3] != d) return fail(WLLM_ERR_INVALID_ARG, "cache head_dim differs from q");
+  if (hkv != num_kv_heads)
+    return fail(WLLM_ERR_INVALID_ARG, "num_kv_heads %d differs from cache dim %lld", num_kv_heads, (long long)hkv);
+  if (bs != block_size)
+    return fail(WLLM_ERR_INVALID_ARG, "block_size %d differs from cache dim %lld", block_size, (long long)bs);
+  if (hkv <= 0 || hq % hkv != 0) return fail(WLLM_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  if (block_tables->shape[0] != B) return fail(WLLM_ERR_INVALID_ARG, "block_tables must have B rows");
+  if (context_lens->shape[0] != B) return fail(WLLM_ERR_INVALID_ARG, "context_lens must have B entries");
+  if (B > 1 && context_lens->stride[0] != 1) return fail(WLLM_ERR_INVALID_ARG, "context_lens must be contiguous");
+  const int64_t mb = block_tables->shape[1];
+  if (mb > 1 && block_tables->stride[1] != 1)
+    return fail(WLLM_ERR_INVALID_ARG, "block_tables rows must be contiguous");
+  if (!contiguous(k_cache) || !contiguous(v_cache)) return fail(WLLM_ERR_INVALID_ARG, "caches must be dense");
+  if (d > 1 && (q->stride[2] != 1 || out->stride[2] != 1))
+    return fail(WLLM_ERR_INVALID_ARG, "q/out last dimension must be contiguous");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(WLLM_ERR_INVALID_ARG, "scale must be finite");
+  if (d != 64 && d != 128 && d != 256)
+    return fail(WLLM_ERR_UNSUPPORTED, "head_dim %lld not supported (64, 128, 256)", (long long)d);
+  if (!is_pow2(bs) || bs < 8 || bs > 256)
+    return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
+  if (B > INT32_MAX || hq > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
+    return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  if (B == 0 || hq == 0) return WLLM_OK;
+  if (nb < 1) return fail(WLLM_ERR_INVALID_ARG, "the pool has no blocks");
+  if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
+    return fail(WLLM_ERR_INVALID_ARG, "cache base pointers must be 16-byte aligned");
+  const int elt = elt_size(dt);
+  if (!(aligned(q->data, 16) && (q->stride[0] * elt) % 16 == 0 && (q->stride[1] * elt) % 16 == 0))
+    return fail(WLLM_ERR_UNSUPPORTED, "the allocation-free decode needs 16-byte aligned query rows");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int num_sms = 0;
+  e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  uint8_t* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  // plan every slice first: reject before launching anything
+  for (int64_t b0 = 0; b0 < B; b0 += kPersistentMaxSeqs) {
+    const int64_t nbat = std::min<int64_t>(kPersistentMaxSeqs, B - b0);
+    const DecodePlan pl = make_plan(dt, nbat, hq, hkv, d, mb, bs, true, num_sms);
+    if (!pl.persistent)
+      return fail(WLLM_ERR_UNSUPPORTED, "the allocation-free decode runs only the persistent tensor-core kernel");
+    const size_t need = pl.ml_bytes + pl.o_bytes;
+    if (need > kNoAllocScratchBytes - kNoAllocControlBytes)
+      return fail(WLLM_ERR_UNSUPPORTED,
+                  "allocation-free decode: these sizes need %zu bytes of split-KV scratch, the fixed array holds %zu",
+                  need, kNoAllocScratchBytes - kNoAllocControlBytes);
+  }
+
+  CUtensorMap kmap, vmap;
+  if ((rc = make_pool_map(&kmap, k_cache->data, dt, nb, hkv, bs, d, "k_cache"))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, dt, nb, hkv, bs, d, "v_cache"))) return rc;
+
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  for (int64_t b0 = 0; b0 < B; b0 += kPersistentMaxSeqs) {
+    const int64_t nbat = std::min<int64_t>(kPersistentMaxSeqs, B - b0);
+    const DecodePlan pl = make_plan(dt, nbat, hq, hkv, d, mb, bs, true, num_sms);
+    // the error and scheduler words must start at zero; partials need no clearing
+    e = cudaMemsetAsync(scratch, 0, kNoAllocControlBytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(control words)");
+    DecodeParams p{};
+    p.out = static_cast<uint8_t*>(out->data) + b0 * out->stride[0] * elt;
+    p.q = static_cast<const uint8_t*>(q->data) + b0 * q->stride[0] * elt;
+    p.q_sb = q->stride[0];
+    p.q_sh = q->stride[1];
+    p.o_sb = out->stride[0];
+    p.o_sh = out->stride[1];
+    p.block_tables = static_cast<const int32_t*>(block_tables->data) + b0 * block_tables->stride[0];
+    p.bt_stride = block_tables->stride[0];
+    p.context_lens = static_cast<const int32_t*>(context_lens->data) + b0;
+    p.num_seqs = static_cast<int>(nbat);
+    p.num_q_heads = static_cast<int>(hq);
+    p.num_kv_heads = static_cast<int>(hkv);
+    p.group = static_cast<int>(hq / hkv);
+    p.head_tile = pl.head_tile;
+    p.num_head_tiles = pl.tiles;
+    p.max_blocks = static_cast<int>(mb);
+    p.block_size = static_cast<int>(bs);
+    p.log2_bs = ilog2(bs);
+    p.num_blocks = static_cast<int>(nb);
+    p.part_tokens = pl.part_tokens;
+    p.max_parts = pl.max_parts;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = reinterpret_cast<int*>(scratch);
+    p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
+    p.ws_count = nullptr;
+    p.ws_ml = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes) : nullptr;
+    p.ws_o = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes + pl.ml_bytes) : nullptr;
+    e = static_cast<cudaError_t>(launch_decode_persistent(dt, static_cast<int>(d), pl.head_tile, kmap, vmap, p,
+                                                          pl.grid, pl.separate_combine, st));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  }
+  return WLLM_OK;
+}
+
 }  // extern "C"

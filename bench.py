@@ -353,7 +353,7 @@ def run_ours(args):
         "pct_of_8tbs": 100.0 * step_bytes / (ms_per_step / 1e3) / 8e12,
         "kernel_ms": {"append": sum(app_ms) / K, "decode": dec_mean,
                       "decode_median": statistics.median(dec_ms)},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_persistent (+ splitkv_combine)", "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": alg},

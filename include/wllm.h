@@ -132,7 +132,10 @@ int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value,
  * Supported: D in {64, 128, 256}.  F16/BF16 use tensor-core QK^T and PV with
  * fp32 accumulation; F32 uses fp32 FMA.  The cache base pointers must be
  * 16-byte aligned.  Long contexts are split over several CTAs and combined on
- * the device (split-KV); this uses the device workspace (see below).
+ * the device (split-KV); this uses the device workspace (see below).  With
+ * F16/BF16 the partitions are merged inside one cooperative launch (every CTA
+ * resident; grid barriers bounded in time), or by a second kernel when the
+ * environment variable WLLM_SEPARATE_COMBINE=1 is set.
  * A block-table entry outside [0, N_b) or a length above M_b*bs is clamped on
  * the device (the output of that sequence is then meaningless) and, in check
  * mode, reported as WLLM_ERR_OUT_OF_RANGE.
@@ -142,6 +145,31 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q,
                                 const wllm_tensor* block_tables,
                                 const wllm_tensor* context_lens, int num_kv_heads,
                                 float scale, int block_size, wllm_stream stream);
+
+/*
+ * One whole decode step: the KV append followed by paged decode attention,
+ * in one launch where the kernel allows it.
+ *
+ * Passages: those of wllm_reshape_and_cache and wllm_paged_attention_decode;
+ * "wLLM" project page, "Features / Core engine" (decode is launch-bound for
+ * small models; its launches are worth removing).
+ *
+ * Arguments are the union of the two calls' arguments, with the same meaning,
+ * layout and checks: key/value/slot_mapping as in wllm_reshape_and_cache,
+ * out/q/block_tables/context_lens/num_kv_heads/scale/block_size as in
+ * wllm_paged_attention_decode, both on the same k_cache/v_cache.  The result is
+ * the same as calling the two in order: every appended row is visible to the
+ * attention.  For F16/BF16 with 16-byte aligned query rows it is one
+ * cooperative launch of the persistent kernel: its CTAs append their share of
+ * the rows, meet at a grid barrier, attend, and -- when sequences are split --
+ * meet again and merge the partitions.  Other inputs run the two calls' kernels
+ * back to back.  T == 0 skips the append; B == 0 skips the attention.
+ */
+int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key,
+                     const wllm_tensor* value, const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                     const wllm_tensor* slot_mapping, const wllm_tensor* block_tables,
+                     const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
+                     wllm_stream stream);
 
 /*
  * Paged decode attention that allocates no device memory.

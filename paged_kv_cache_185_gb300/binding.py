@@ -21,7 +21,7 @@ WLLM_OK, WLLM_ERR_INVALID_ARG, WLLM_ERR_UNSUPPORTED, WLLM_ERR_OUT_OF_RANGE, WLLM
 _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3, torch.int64: 4}
 
 # every symbol include/wllm.h declares
-EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode",
+EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode", "wllm_decode_step",
             "wllm_paged_attention_decode_noalloc",
             "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
             "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version")
@@ -63,6 +63,9 @@ def load_library():
         lib.wllm_paged_attention_decode.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
                                                     ctypes.c_int, ctypes.c_void_p]
         lib.wllm_paged_attention_decode.restype = ctypes.c_int
+        lib.wllm_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                         ctypes.c_void_p]
+        lib.wllm_decode_step.restype = ctypes.c_int
         lib.wllm_paged_attention_decode_noalloc.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
                                                             ctypes.c_int, ctypes.c_void_p]
         lib.wllm_paged_attention_decode_noalloc.restype = ctypes.c_int
@@ -151,11 +154,16 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
 
 def decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens,
                 num_kv_heads: int, scale: float, block_size: int) -> torch.Tensor:
-    """One decode step of one layer: append this step's K/V, then attend."""
-    if slot_mapping.numel() > 0:
-        reshape_and_cache(key, value, k_cache, v_cache, slot_mapping)
-    return paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
-                                  num_kv_heads, scale, block_size)
+    """One decode step of one layer: append this step's K/V, then attend (one
+    fused launch where the kernel allows; see wllm_decode_step)."""
+    dev = _require_cuda(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (out, q, key, value, k_cache, v_cache, slot_mapping, block_tables,
+                                      context_lens)]
+        _check(lib.wllm_decode_step(*[ctypes.byref(a) for a in args], int(num_kv_heads), float(scale),
+                                    int(block_size), _stream_handle(dev)))
+    return out
 
 
 def workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, block_size) -> int:

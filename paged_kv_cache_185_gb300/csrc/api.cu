@@ -26,20 +26,22 @@ int threads_decode_bf16(int);
 int threads_decode_f16(int);
 int threads_decode_f32(int);
 int launch_persistent_bf16(int, int, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, bool,
-                           cudaStream_t);
+                           const AppendParams*, bool, cudaStream_t);
 int launch_persistent_f16(int, int, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, bool,
-                          cudaStream_t);
+                          const AppendParams*, bool, cudaStream_t);
 int occupancy_persistent_bf16(int, int, int);
 int occupancy_persistent_f16(int, int, int);
 
 int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
-                             cudaStream_t stream) {
+                             const AppendParams* ap, bool fuse_combine, cudaStream_t stream) {
   switch (dtype) {
     case WLLM_BF16:
-      return launch_persistent_bf16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, stream);
+      return launch_persistent_bf16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, ap, fuse_combine,
+                                    stream);
     case WLLM_F16:
-      return launch_persistent_f16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, stream);
+      return launch_persistent_f16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, ap, fuse_combine,
+                                   stream);
     default:
       return cudaErrorInvalidValue;
   }
@@ -366,8 +368,14 @@ const char* wllm_last_error(void) { return g_last_error.c_str(); }
 
 const char* wllm_version(void) { return "wllm-gb300 0.1.0 (sm_103a)"; }
 
-int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
-                           const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, wllm_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// Check the append arguments and fill `ap` (all but the error word).  Leaves
+// ap.num_tokens == 0 when there is nothing to write.
+int prepare_append(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
+                   const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, AppendParams& ap) {
   int rc;
   if ((rc = check_desc(key, "key", 3)) || (rc = check_desc(value, "value", 3)) ||
       (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
@@ -395,43 +403,56 @@ int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, con
   if (!is_pow2(bs)) return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld is not a power of two", (long long)bs);
   if (T > INT32_MAX || hkv > INT32_MAX || d * elt_size(dt) > INT32_MAX)
     return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  ap = AppendParams{};
   if (T == 0 || hkv == 0 || d == 0) return WLLM_OK;
+  const int elt = elt_size(dt);
+  ap.key = static_cast<const uint8_t*>(key->data);
+  ap.value = static_cast<const uint8_t*>(value->data);
+  ap.k_cache = static_cast<uint8_t*>(k_cache->data);
+  ap.v_cache = static_cast<uint8_t*>(v_cache->data);
+  ap.slots = slot_mapping->data;
+  ap.slots_are_i64 = slot_mapping->dtype == WLLM_I64;
+  ap.num_tokens = static_cast<int>(T);
+  ap.num_kv_heads = static_cast<int>(hkv);
+  ap.row_bytes = static_cast<int>(d * elt);
+  ap.key_st = key->stride[0] * elt;
+  ap.key_sh = key->stride[1] * elt;
+  ap.val_st = value->stride[0] * elt;
+  ap.val_sh = value->stride[1] * elt;
+  ap.log2_bs = ilog2(bs);
+  ap.num_slots = nb * bs;
+  ap.vec16 = (ap.row_bytes % 16 == 0) && aligned(ap.key, 16) && aligned(ap.value, 16) && aligned(ap.k_cache, 16) &&
+             aligned(ap.v_cache, 16) && ap.key_st % 16 == 0 && ap.key_sh % 16 == 0 && ap.val_st % 16 == 0 &&
+             ap.val_sh % 16 == 0;
+  if (!ap.vec16 && !(aligned(ap.key, 2) && aligned(ap.value, 2)))
+    return fail(WLLM_ERR_INVALID_ARG, "key/value must be at least 2-byte aligned");
+  return WLLM_OK;
+}
 
+// Check-mode pass over the slots (bounds, duplicates): synchronising.
+int check_append_slots(DeviceState* s, const AppendParams& ap, cudaStream_t st) {
+  cudaError_t e = static_cast<cudaError_t>(
+      launch_check_append(ap.slots, ap.slots_are_i64, ap.num_tokens, ap.num_slots, s->err, st));
+  if (e != cudaSuccess) return cuda_fail(e, "check_append launch");
+  return collect_device_errors(s, st, "reshape_and_cache");
+}
+
+}  // namespace
+
+extern "C" {
+
+int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
+                           const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, wllm_stream stream) {
+  AppendParams ap{};
+  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap);
+  if (rc || ap.num_tokens == 0) return rc;
   DeviceState* s = nullptr;
   if ((rc = device_state(&s))) return rc;
-  const int elt = elt_size(dt);
-  AppendParams p{};
-  p.key = static_cast<const uint8_t*>(key->data);
-  p.value = static_cast<const uint8_t*>(value->data);
-  p.k_cache = static_cast<uint8_t*>(k_cache->data);
-  p.v_cache = static_cast<uint8_t*>(v_cache->data);
-  p.slots = slot_mapping->data;
-  p.slots_are_i64 = slot_mapping->dtype == WLLM_I64;
-  p.num_tokens = static_cast<int>(T);
-  p.num_kv_heads = static_cast<int>(hkv);
-  p.row_bytes = static_cast<int>(d * elt);
-  p.key_st = key->stride[0] * elt;
-  p.key_sh = key->stride[1] * elt;
-  p.val_st = value->stride[0] * elt;
-  p.val_sh = value->stride[1] * elt;
-  p.log2_bs = ilog2(bs);
-  p.num_slots = nb * bs;
-  p.vec16 = (p.row_bytes % 16 == 0) && aligned(p.key, 16) && aligned(p.value, 16) && aligned(p.k_cache, 16) &&
-            aligned(p.v_cache, 16) && p.key_st % 16 == 0 && p.key_sh % 16 == 0 && p.val_st % 16 == 0 &&
-            p.val_sh % 16 == 0;
-  if (!p.vec16 && !(aligned(p.key, 2) && aligned(p.value, 2)))
-    return fail(WLLM_ERR_INVALID_ARG, "key/value must be at least 2-byte aligned");
-  p.err = s->err;
-
+  ap.err = s->err;
   const bool check = env_flag("WLLM_CHECK");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (check) {
-    cudaError_t e = static_cast<cudaError_t>(launch_check_append(p.slots, p.slots_are_i64, p.num_tokens,
-                                                                 p.num_slots, s->err, st));
-    if (e != cudaSuccess) return cuda_fail(e, "check_append launch");
-    if ((rc = collect_device_errors(s, st, "reshape_and_cache"))) return rc;
-  }
-  cudaError_t e = static_cast<cudaError_t>(launch_append(p, st));
+  if (check && (rc = check_append_slots(s, ap, st))) return rc;
+  cudaError_t e = static_cast<cudaError_t>(launch_append(ap, st));
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   if (check) return collect_device_errors(s, st, "reshape_and_cache");
   return WLLM_OK;
@@ -543,10 +564,20 @@ int bind_workspace(DeviceState* s, const DecodePlan& pl, cudaStream_t st, Decode
 
 }  // namespace
 
-int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
-                                const wllm_tensor* v_cache, const wllm_tensor* block_tables,
-                                const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
-                                wllm_stream stream) {
+}  // extern "C"
+
+namespace {
+
+struct DecodeArgs {
+  int dt = 0, elt = 0;
+  int64_t B = 0, hq = 0, d = 0, nb = 0, hkv = 0, bs = 0, mb = 0;
+  bool q_bulk_ok = false;
+};
+
+// Check the decode arguments; a.B == 0 (or no heads) means nothing to do.
+int prepare_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                   const wllm_tensor* v_cache, const wllm_tensor* block_tables, const wllm_tensor* context_lens,
+                   int num_kv_heads, float scale, int block_size, DecodeArgs& a) {
   int rc;
   if ((rc = check_desc(out, "out", 3)) || (rc = check_desc(q, "q", 3)) ||
       (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
@@ -585,45 +616,57 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, co
     return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
   if (B > INT32_MAX || hq > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
     return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  a = DecodeArgs{};
+  a.dt = dt;
+  a.B = B;
+  a.hq = hq;
   if (B == 0 || hq == 0) return WLLM_OK;
   if (nb < 1) return fail(WLLM_ERR_INVALID_ARG, "the pool has no blocks");
   if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
     return fail(WLLM_ERR_INVALID_ARG, "cache base pointers must be 16-byte aligned");
   const int elt = elt_size(dt);
-  const bool q_bulk_ok = aligned(q->data, 16) && (q->stride[0] * elt) % 16 == 0 && (q->stride[1] * elt) % 16 == 0;
   if (dt != WLLM_F32 && !(aligned(q->data, 4) && q->stride[0] % 2 == 0 && q->stride[1] % 2 == 0))
     return fail(WLLM_ERR_INVALID_ARG, "q rows must be 4-byte aligned");
+  a.elt = elt;
+  a.d = d;
+  a.nb = nb;
+  a.hkv = hkv;
+  a.bs = bs;
+  a.mb = mb;
+  a.q_bulk_ok = aligned(q->data, 16) && (q->stride[0] * elt) % 16 == 0 && (q->stride[1] * elt) % 16 == 0;
+  return WLLM_OK;
+}
 
-  std::lock_guard<std::mutex> lock(g_mutex);
-  DeviceState* s = nullptr;
-  if ((rc = device_state(&s))) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
+// Launch the decode (slices of at most kPersistentMaxSeqs sequences for the
+// persistent kernel).  `fuse_ap` non-null runs the KV append inside the first
+// persistent launch.  Caller holds g_mutex.
+int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+               const wllm_tensor* v_cache, const wllm_tensor* block_tables, const wllm_tensor* context_lens,
+               float scale, DeviceState* s, cudaStream_t st, const AppendParams* fuse_ap) {
+  int rc;
   CUtensorMap kmap, vmap;
-  if ((rc = make_pool_map(&kmap, k_cache->data, dt, nb, hkv, bs, d, "k_cache"))) return rc;
-  if ((rc = make_pool_map(&vmap, v_cache->data, dt, nb, hkv, bs, d, "v_cache"))) return rc;
-
+  if ((rc = make_pool_map(&kmap, k_cache->data, a.dt, a.nb, a.hkv, a.bs, a.d, "k_cache"))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, a.dt, a.nb, a.hkv, a.bs, a.d, "v_cache"))) return rc;
   const bool check = env_flag("WLLM_CHECK");
   if (check) {
     cudaError_t e = static_cast<cudaError_t>(launch_check_decode(
         static_cast<const int32_t*>(block_tables->data), block_tables->stride[0],
-        static_cast<const int32_t*>(context_lens->data), static_cast<int>(B), static_cast<int>(mb),
-        static_cast<int>(bs), static_cast<int>(nb), s->err, st));
+        static_cast<const int32_t*>(context_lens->data), static_cast<int>(a.B), static_cast<int>(a.mb),
+        static_cast<int>(a.bs), static_cast<int>(a.nb), s->err, st));
     if (e != cudaSuccess) return cuda_fail(e, "check_decode launch");
     if ((rc = collect_device_errors(s, st, "paged_attention_decode"))) return rc;
   }
-
-  // the persistent kernel keeps per-sequence prefix sums in shared memory, so
-  // very large batches go in slices of kPersistentMaxSeqs sequences
-  const DecodePlan first = make_plan(dt, std::min<int64_t>(B, kPersistentMaxSeqs), hq, hkv, d, mb, bs, q_bulk_ok,
-                                     s->num_sms);
-  const int64_t slice = first.persistent ? kPersistentMaxSeqs : B;
-  for (int64_t b0 = 0; b0 < B; b0 += slice) {
-    const int64_t nbat = std::min<int64_t>(slice, B - b0);
-    const DecodePlan pl = make_plan(dt, nbat, hq, hkv, d, mb, bs, q_bulk_ok, s->num_sms);
+  // split partitions are merged inside the (cooperative) launch unless asked otherwise
+  const bool separate_kernel = env_flag("WLLM_SEPARATE_COMBINE");
+  const DecodePlan first = make_plan(a.dt, std::min<int64_t>(a.B, kPersistentMaxSeqs), a.hq, a.hkv, a.d, a.mb,
+                                     a.bs, a.q_bulk_ok, s->num_sms);
+  const int64_t slice = first.persistent ? kPersistentMaxSeqs : a.B;
+  for (int64_t b0 = 0; b0 < a.B; b0 += slice) {
+    const int64_t nbat = std::min<int64_t>(slice, a.B - b0);
+    const DecodePlan pl = make_plan(a.dt, nbat, a.hq, a.hkv, a.d, a.mb, a.bs, a.q_bulk_ok, s->num_sms);
     DecodeParams p{};
-    p.out = static_cast<uint8_t*>(out->data) + b0 * out->stride[0] * elt;
-    p.q = static_cast<const uint8_t*>(q->data) + b0 * q->stride[0] * elt;
+    p.out = static_cast<uint8_t*>(out->data) + b0 * out->stride[0] * a.elt;
+    p.q = static_cast<const uint8_t*>(q->data) + b0 * q->stride[0] * a.elt;
     p.q_sb = q->stride[0];
     p.q_sh = q->stride[1];
     p.o_sb = out->stride[0];
@@ -632,32 +675,83 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, co
     p.bt_stride = block_tables->stride[0];
     p.context_lens = static_cast<const int32_t*>(context_lens->data) + b0;
     p.num_seqs = static_cast<int>(nbat);
-    p.num_q_heads = static_cast<int>(hq);
-    p.num_kv_heads = static_cast<int>(hkv);
-    p.group = static_cast<int>(hq / hkv);
+    p.num_q_heads = static_cast<int>(a.hq);
+    p.num_kv_heads = static_cast<int>(a.hkv);
+    p.group = static_cast<int>(a.hq / a.hkv);
     p.head_tile = pl.head_tile;
     p.num_head_tiles = pl.tiles;
-    p.max_blocks = static_cast<int>(mb);
-    p.block_size = static_cast<int>(bs);
-    p.log2_bs = ilog2(bs);
-    p.num_blocks = static_cast<int>(nb);
+    p.max_blocks = static_cast<int>(a.mb);
+    p.block_size = static_cast<int>(a.bs);
+    p.log2_bs = ilog2(a.bs);
+    p.num_blocks = static_cast<int>(a.nb);
     p.part_tokens = pl.part_tokens;
     p.max_parts = pl.max_parts;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = s->err;
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
-    if (!pl.persistent && hkv * pl.tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
+    if (!pl.persistent && a.hkv * pl.tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
     if ((rc = bind_workspace(s, pl, st, p))) return rc;
     cudaError_t e;
-    if (pl.persistent)
-      e = static_cast<cudaError_t>(launch_decode_persistent(dt, static_cast<int>(d), pl.head_tile, kmap, vmap, p,
-                                                            pl.grid, pl.separate_combine, st));
-    else
-      e = static_cast<cudaError_t>(launch_decode(dt, static_cast<int>(d), pl.variant, kmap, vmap, p, st));
+    if (pl.persistent) {
+      const AppendParams* ap = b0 == 0 ? fuse_ap : nullptr;
+      const bool fuse_combine = pl.max_parts > 1 && !separate_kernel;
+      e = static_cast<cudaError_t>(launch_decode_persistent(a.dt, static_cast<int>(a.d), pl.head_tile, kmap, vmap,
+                                                            p, pl.grid, pl.separate_combine, ap, fuse_combine, st));
+    } else {
+      if (b0 == 0 && fuse_ap != nullptr) {  // no fused form for this kernel: append first
+        e = static_cast<cudaError_t>(launch_append(*fuse_ap, st));
+        if (e != cudaSuccess) return cuda_fail(e, "append launch");
+      }
+      e = static_cast<cudaError_t>(launch_decode(a.dt, static_cast<int>(a.d), pl.variant, kmap, vmap, p, st));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   if (check) return collect_device_errors(s, st, "paged_attention_decode");
   return WLLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
+                                wllm_stream stream) {
+  DecodeArgs a;
+  int rc = prepare_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, a);
+  if (rc || a.B == 0 || a.hq == 0) return rc;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s))) return rc;
+  return run_decode(a, out, q, k_cache, v_cache, block_tables, context_lens, scale, s,
+                    reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key, const wllm_tensor* value,
+                     const wllm_tensor* k_cache, const wllm_tensor* v_cache, const wllm_tensor* slot_mapping,
+                     const wllm_tensor* block_tables, const wllm_tensor* context_lens, int num_kv_heads, float scale,
+                     int block_size, wllm_stream stream) {
+  AppendParams ap{};
+  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap);
+  if (rc) return rc;
+  DecodeArgs a;
+  if ((rc = prepare_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, a)))
+    return rc;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ap.err = s->err;
+  const bool have_append = ap.num_tokens > 0;
+  if (have_append && env_flag("WLLM_CHECK") && (rc = check_append_slots(s, ap, st))) return rc;
+  if (a.B == 0 || a.hq == 0) {  // nothing to attend: the append alone
+    if (!have_append) return WLLM_OK;
+    cudaError_t e = static_cast<cudaError_t>(launch_append(ap, st));
+    return e == cudaSuccess ? WLLM_OK : cuda_fail(e, "append launch");
+  }
+  return run_decode(a, out, q, k_cache, v_cache, block_tables, context_lens, scale, s, st,
+                    have_append ? &ap : nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -818,7 +912,7 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
     p.ws_ml = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes) : nullptr;
     p.ws_o = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes + pl.ml_bytes) : nullptr;
     e = static_cast<cudaError_t>(launch_decode_persistent(dt, static_cast<int>(d), pl.head_tile, kmap, vmap, p,
-                                                          pl.grid, pl.separate_combine, st));
+                                                          pl.grid, pl.separate_combine, nullptr, false, st));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return WLLM_OK;

@@ -9,6 +9,7 @@
 // [num_blocks][num_kv_heads][block_size][head_dim].  The copy moves raw bits
 // (16-byte vectors when rows and strides allow), so it is bit-exact for every
 // element type.
+#include "append_row.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -18,44 +19,10 @@ namespace {
 
 constexpr int kAppendWarps = 8;
 
-template <bool kVec16>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p) {
-  const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
   if (gw >= static_cast<int64_t>(p.num_tokens) * p.num_kv_heads) return;
-  const int t = static_cast<int>(gw / p.num_kv_heads);
-  const int h = static_cast<int>(gw - static_cast<int64_t>(t) * p.num_kv_heads);
-  const int64_t slot = p.slots_are_i64 ? static_cast<const int64_t*>(p.slots)[t]
-                                       : static_cast<int64_t>(static_cast<const int32_t*>(p.slots)[t]);
-  if (slot < 0) return;  // padding token
-  if (slot >= p.num_slots) {
-    if (lane == 0) atomicOr(p.err, kErrSlot);
-    return;
-  }
-  const int64_t blk = slot >> p.log2_bs;
-  const int64_t off = slot & ((int64_t(1) << p.log2_bs) - 1);
-  const int64_t dst = (((blk * p.num_kv_heads + h) << p.log2_bs) + off) * p.row_bytes;
-  const uint8_t* ks = p.key + t * p.key_st + h * p.key_sh;
-  const uint8_t* vs = p.value + t * p.val_st + h * p.val_sh;
-  uint8_t* kd = p.k_cache + dst;
-  uint8_t* vd = p.v_cache + dst;
-  if constexpr (kVec16) {
-    const int n = p.row_bytes >> 4;  // 16-byte units per row
-    for (int u = lane; u < 2 * n; u += 32) {
-      if (u < n)
-        reinterpret_cast<uint4*>(kd)[u] = reinterpret_cast<const uint4*>(ks)[u];
-      else
-        reinterpret_cast<uint4*>(vd)[u - n] = reinterpret_cast<const uint4*>(vs)[u - n];
-    }
-  } else {
-    const int n = p.row_bytes >> 1;  // 2-byte units (every supported element is 2 or 4 bytes)
-    for (int u = lane; u < 2 * n; u += 32) {
-      if (u < n)
-        reinterpret_cast<uint16_t*>(kd)[u] = reinterpret_cast<const uint16_t*>(ks)[u];
-      else
-        reinterpret_cast<uint16_t*>(vd)[u - n] = reinterpret_cast<const uint16_t*>(vs)[u - n];
-    }
-  }
+  append_row(p, gw, threadIdx.x & 31);
 }
 
 __global__ void check_decode_kernel(const int32_t* block_tables, int64_t bt_stride,
@@ -99,10 +66,7 @@ int launch_append(const AppendParams& p, cudaStream_t stream) {
   const int64_t warps = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads;
   const int64_t blocks = (warps + kAppendWarps - 1) / kAppendWarps;
   if (blocks == 0) return cudaSuccess;
-  if (p.vec16)
-    append_kernel<true><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
-  else
-    append_kernel<false><<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
+  append_kernel<<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,49 @@
+// append_row.cuh -- one (token, kv head) row of the KV append, done by one
+// warp: the token's K row and V row (head_dim elements each) are copied bit
+// for bit into slot slot_mapping[t] of the caches.  Shared by the append
+// kernel and the fused decode step.
+#pragma once
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace wllm {
+
+// Row `row` = t * num_kv_heads + h.  All 32 lanes of the warp call this.
+__device__ __forceinline__ void append_row(const AppendParams& p, int64_t row, int lane) {
+  const int t = static_cast<int>(row / p.num_kv_heads);
+  const int h = static_cast<int>(row - static_cast<int64_t>(t) * p.num_kv_heads);
+  const int64_t slot = p.slots_are_i64 ? static_cast<const int64_t*>(p.slots)[t]
+                                       : static_cast<int64_t>(static_cast<const int32_t*>(p.slots)[t]);
+  if (slot < 0) return;  // padding token
+  if (slot >= p.num_slots) {
+    if (lane == 0) atomicOr(p.err, kErrSlot);
+    return;
+  }
+  const int64_t blk = slot >> p.log2_bs;
+  const int64_t off = slot & ((int64_t(1) << p.log2_bs) - 1);
+  const int64_t dst = (((blk * p.num_kv_heads + h) << p.log2_bs) + off) * p.row_bytes;
+  const uint8_t* ks = p.key + t * p.key_st + h * p.key_sh;
+  const uint8_t* vs = p.value + t * p.val_st + h * p.val_sh;
+  uint8_t* kd = p.k_cache + dst;
+  uint8_t* vd = p.v_cache + dst;
+  if (p.vec16) {
+    const int n = p.row_bytes >> 4;  // 16-byte units per row
+    for (int u = lane; u < 2 * n; u += 32) {
+      if (u < n)
+        reinterpret_cast<uint4*>(kd)[u] = reinterpret_cast<const uint4*>(ks)[u];
+      else
+        reinterpret_cast<uint4*>(vd)[u - n] = reinterpret_cast<const uint4*>(vs)[u - n];
+    }
+  } else {
+    const int n = p.row_bytes >> 1;  // 2-byte units (every supported element is 2 or 4 bytes)
+    for (int u = lane; u < 2 * n; u += 32) {
+      if (u < n)
+        reinterpret_cast<uint16_t*>(kd)[u] = reinterpret_cast<const uint16_t*>(ks)[u];
+      else
+        reinterpret_cast<uint16_t*>(vd)[u - n] = reinterpret_cast<const uint16_t*>(vs)[u - n];
+    }
+  }
+}
+
+}  // namespace wllm

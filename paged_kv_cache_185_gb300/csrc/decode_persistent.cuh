@@ -34,13 +34,47 @@
 // between launches.
 #pragma once
 
+#include "append_row.cuh"
 #include "decode_kernel.cuh"
 
 namespace wllm {
 
-// the scheduler words live next to the error word (offsets in ints)
+// the scheduler and grid-barrier words live next to the error word (offsets in ints)
 constexpr int kSchedNextOffset = 16;
 constexpr int kSchedDoneOffset = 32;
+constexpr int kGridCountOffset = 48;
+constexpr int kGridGenOffset = 56;
+
+// fused-step flags of one launch
+enum : int { kFuseAppend = 1, kFuseCombine = 2 };
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Bounded grid-wide rendezvous, called by one thread per CTA.  The launch is
+// cooperative, so every CTA is resident and the barrier cannot deadlock; it
+// still gives up after limit_ns (returns false) rather than spin forever.  The
+// generation word only grows, so no reset is needed between launches.
+__device__ __forceinline__ bool grid_barrier(int* ctrl, uint64_t limit_ns) {
+  volatile int* gen_p = ctrl + kGridGenOffset;
+  int* count = ctrl + kGridCountOffset;
+  const int gen = *gen_p;
+  __threadfence();
+  if (atomicAdd(count, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(count, 0);
+    __threadfence();
+    atomicAdd(ctrl + kGridGenOffset, 1);
+    return true;
+  }
+  const uint64_t t0 = global_timer_ns();
+  while (*gen_p == gen) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  __threadfence();
+  return true;
+}
 
 struct StageMeta {
   int b, p, t0, tok_end;
@@ -113,6 +147,61 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, int& phase, uint64_t
   return __all_sync(kFullMask, ok);
 }
 
+// Merge the partitions of one query row (b, h): weights exp2(m_p - M), fp32
+// sums, round-to-nearest into `out`.  One warp; rows with one partition were
+// written by the decode itself.
+template <typename T, int D>
+__device__ __forceinline__ void combine_row(const DecodeParams& p, int row, int lane) {
+  const int b = row / p.num_q_heads;
+  int L = p.context_lens[b];
+  const int l_max = p.max_blocks * p.block_size;
+  L = L < 0 ? 0 : (L > l_max ? l_max : L);
+  const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  if (n_parts == 1) return;
+  const int64_t base = static_cast<int64_t>(row) * p.max_parts;
+  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml);
+  float M = -INFINITY;
+  for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(ml + base + pp).x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+  float den = 0.f, num[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
+  for (int p0 = 0; p0 < n_parts; p0 += 32) {
+    const bool mine = p0 + lane < n_parts;
+    const float2 v = mine ? __ldcg(ml + base + p0 + lane) : make_float2(-INFINITY, 0.f);
+    const float f = mine ? exp2f(v.x - M) : 0.f;
+    den += f * v.y;
+    const int cnt = min(32, n_parts - p0);
+    // eight partitions per batch, every load issued before the first use
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float o[8][D / 32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j0 + j < cnt) {
+          const float* src = p.ws_o + (base + p0 + j0 + j) * D;
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) o[j][i] = __ldcg(src + lane + 32 * i);
+        }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float fp = __shfl_sync(kFullMask, f, (j0 + j) & 31);
+        if (j0 + j < cnt) {
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) num[i] = fmaf(fp, o[j][i], num[i]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
+  const float inv = 1.f / den;
+  const int h = row - b * p.num_q_heads;
+  T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
+}
+
 struct UnitInfo {
   int b, part, z, n_parts, tb, te, n_chunks, kvh, h0, nh;
 };
@@ -120,7 +209,7 @@ struct UnitInfo {
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     paged_decode_persistent(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                            const DecodeParams p) {
+                            const DecodeParams p, const AppendParams ap, const int flags) {
   using G = Geom<T, D>;
   using PS = PShape<T, D, NT>;
   constexpr int S = PS::kStages;
@@ -156,6 +245,26 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   }
   __syncthreads();
   const int BZ = B * Z;  // partition-0 units
+
+  // fused step: this CTA's share of the KV append, made visible to the other
+  // CTAs' tensor copies before any of them reads the cache (grid barrier below)
+  if (flags & kFuseAppend) {
+    const int64_t rows = static_cast<int64_t>(ap.num_tokens) * ap.num_kv_heads;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (W + 1) + warp; r < rows;
+         r += static_cast<int64_t>(gridDim.x) * (W + 1))
+      append_row(ap, r, lane);
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  bool failed = false;  // a bounded wait gave up: skip to the end, still meet every barrier
+  auto cta_grid_sync = [&]() -> bool {
+    named_barrier_sync(2, PS::kThreads);
+    if (threadIdx.x == 0) wsum[8] = grid_barrier(p.err, p.wait_limit_ns) ? 1 : 0;
+    named_barrier_sync(2, PS::kThreads);
+    const bool ok_ = wsum[8] != 0;
+    if (!ok_ && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return ok_;
+  };
 
   if (warp == W) {
     // ------------------------------- producer -------------------------------
@@ -266,6 +375,9 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     bool have_cur = decode_unit(static_cast<int>(blockIdx.x), cur, e0, e1);
     int raw_next = 0;
     if (lane == 0 && have_cur) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+    if (flags & kFuseAppend) {  // no cache read before every CTA's append is done
+      if (!cta_grid_sync()) ok = false;
+    }
     while (ok && have_cur) {
       // the next unit is fetched once the current one has filled the ring
       // (or has no more stages), so its latency overlaps the copies in flight
@@ -383,8 +495,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         atomicExch(sched_done, 0);
       }
     }
-    return;
-  }
+    failed = !ok;
+  } else {
 
   // ------------------------------- consumers --------------------------------
   // prefix sums of the units at partitions >= 1, sequence-major, and the
@@ -419,6 +531,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
     if (threadIdx.x == 0) mbar_arrive(smem_u32(pbar));
   }
+  if ((flags & kFuseAppend) && !cta_grid_sync()) failed = true;
   MmaState<T, D, NT> st;
   const int cw = warp;
   float* red_o = reinterpret_cast<float*>(red_area);  // [W][HT][D]
@@ -427,14 +540,15 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   const uint32_t sync_bar = smem_u32(cbar);
   int sync_phase = 0;
   T* out = reinterpret_cast<T*>(p.out);
-  for (int k = 0;; ++k) {
+  for (int k = 0; !failed; ++k) {
     const int s = k % S;
     if (!mbar_wait_bounded(smem_u32(full + s), (k / S) & 1, p.wait_limit_ns)) {
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-      return;
+      failed = true;
+      break;
     }
     const StageMeta mt_ = meta[s];
-    if (mt_.flags & kStop) return;
+    if (mt_.flags & kStop) break;
     const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
     if (!(mt_.flags & kEmptySeq)) {
       if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, ring + s * PS::kStageBytes + 2 * kSub * PS::kKV, mt_.nh, lane);
@@ -458,7 +572,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     mma_store<T, D, NT>(st, red_o + cw * HT * D, red_m + cw * HT, red_l + cw * HT, lane);
     if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-      return;
+      failed = true;
+      break;
     }
     const bool split = mt_.n_parts > 1;
     const int row0 = b * p.num_q_heads + h0;
@@ -502,54 +617,30 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     }
     if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {  // reduction area free again
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-      return;
+      failed = true;
+      break;
+    }
+  }
+  }  // consumers
+
+  // fused step: once every CTA's partials are written, all warps of all CTAs
+  // merge the split rows (one warp per query row)
+  if (flags & kFuseCombine) {
+    if (cta_grid_sync() && !failed) {
+      const int gwarp = static_cast<int>(blockIdx.x) * (W + 1) + warp;
+      for (int row = gwarp; row < B * p.num_q_heads; row += static_cast<int>(gridDim.x) * (W + 1))
+        combine_row<T, D>(p, row, lane);
     }
   }
 }
 
-// Combine kernel for launches that split sequences into partitions: one warp per
-// query row (b, h); lanes hold the partitions' weights and the output columns.
+// Combine kernel for launches that split sequences into partitions: one warp
+// per query row.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + warp;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= p.num_seqs * p.num_q_heads) return;
-  const int b = row / p.num_q_heads;
-  int L = p.context_lens[b];
-  const int l_max = p.max_blocks * p.block_size;
-  L = L < 0 ? 0 : (L > l_max ? l_max : L);
-  const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-  if (n_parts == 1) return;  // written by the decode kernel
-  const int64_t base = static_cast<int64_t>(row) * p.max_parts;
-  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml);
-  float M = -INFINITY;
-  for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, ml[base + pp].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
-  float den = 0.f, num[D / 32];
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
-  for (int p0 = 0; p0 < n_parts; p0 += 32) {
-    const bool mine = p0 + lane < n_parts;
-    const float2 v = mine ? ml[base + p0 + lane] : make_float2(-INFINITY, 0.f);
-    const float f = mine ? exp2f(v.x - M) : 0.f;
-    den += f * v.y;
-    const int cnt = min(32, n_parts - p0);
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const float fp = __shfl_sync(kFullMask, f, j);
-      const float* o = p.ws_o + (base + p0 + j) * D;
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) num[i] = fmaf(fp, o[lane + 32 * i], num[i]);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
-  const float inv = 1.f / den;
-  const int h = row - b * p.num_q_heads;
-  T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh;
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
+  combine_row<T, D>(p, row, threadIdx.x & 31);
 }
 
 template <typename T, int D, int NT>
@@ -557,9 +648,15 @@ int persistent_smem(int num_seqs) {
   return PShape<T, D, NT>::kFixedSmem + ((2 * num_seqs + 1) * 4 + 15) / 16 * 16;
 }
 
+// Launch the persistent decode.  `ap` non-null fuses the KV append in front of
+// the decode; `fuse_combine` merges split partitions inside the launch.  Either
+// makes the launch cooperative (grid barriers need every CTA resident; the grid
+// never exceeds SMs x occupancy).  Otherwise split partitions are merged by
+// the separate combine kernel when `separate_combine` is set.
 template <typename T, int D, int NT>
 int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p, int grid,
-                           bool separate_combine, cudaStream_t stream) {
+                           bool separate_combine, const AppendParams* ap, bool fuse_combine,
+                           cudaStream_t stream) {
   using PS = PShape<T, D, NT>;
   auto kernel = paged_decode_persistent<T, D, NT>;
   const int smem = persistent_smem<T, D, NT>(p.num_seqs);
@@ -572,9 +669,23 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     if (e != cudaSuccess) return e;
     configured_for[dev] = 227 * 1024;
   }
-  kernel<<<grid, PS::kThreads, smem, stream>>>(kmap, vmap, p);
+  AppendParams none{};
+  const AppendParams& app = ap != nullptr ? *ap : none;
+  const int flags = (ap != nullptr ? kFuseAppend : 0) | (fuse_combine ? kFuseCombine : 0);
+  if (flags == 0) {
+    kernel<<<grid, PS::kThreads, smem, stream>>>(kmap, vmap, p, app, flags);
+  } else {
+    CUtensorMap km = kmap, vm = vmap;
+    DecodeParams pp = p;
+    AppendParams aa = app;
+    int ff = flags;
+    void* args[] = {&km, &vm, &pp, &aa, &ff};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(PS::kThreads), args,
+                                    smem, stream);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaGetLastError();
-  if (e != cudaSuccess || !separate_combine) return e;
+  if (e != cudaSuccess || !separate_combine || fuse_combine) return e;
   splitkv_combine<T, D><<<(p.num_seqs * p.num_q_heads + 7) / 8, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -59,9 +59,11 @@ int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& k
 // Persistent warp-specialised decode (f16/bf16 only).  `separate_combine`
 // appends the split-KV combine kernel (needed when a sequence can span
 // several partitions).
+// `ap` (may be null) fuses the KV append in front; `fuse_combine` merges the
+// partitions inside the launch (both make it a cooperative launch).
 int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
-                             cudaStream_t stream);
+                             const AppendParams* ap, bool fuse_combine, cudaStream_t stream);
 int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs);
 constexpr int kPersistentConsumers = 4;
 constexpr int kPersistentMaxSeqs = 1024;      // sequences per launch (the host splits larger batches)

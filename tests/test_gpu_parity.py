@@ -381,3 +381,83 @@ def test_repeated_launches_leave_scheduler_clean():
                                     4, case.scale, 16)
         torch.cuda.synchronize()
         assert torch.equal(int_view(out.cpu()), int_view(first))
+
+
+# ---------------------------------------------------------------------------
+# the fused decode step (append + decode + combine in one launch)
+# ---------------------------------------------------------------------------
+
+def fused_step(case, pools=None):
+    kc, vc = pools if pools is not None else case.pool("cuda")
+    q = case.q.cuda()
+    out = torch.empty_like(q)
+    wllm.decode_step(out, q, case.key.cuda(), case.value.cuda(), kc, vc, case.slot_mapping.cuda(),
+                     case.block_tables.cuda(), case.context_lens.cuda(), case.num_kv_heads, case.scale,
+                     case.block_size)
+    torch.cuda.synchronize()
+    return out.cpu(), kc, vc
+
+
+@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3"])
+def test_fused_step_matches_oracle(name):
+    case = workloads.make_case(name)
+    got, kc, vc = fused_step(case)
+    ref, kr, vr = oracle_step(case)
+    assert torch.equal(int_view(kc.cpu()), int_view(kr)), "K append not bit-exact"
+    assert torch.equal(int_view(vc.cpu()), int_view(vr)), "V append not bit-exact"
+    del kc, vc
+    assert_attention_close(got, ref, case.dtype, f"fused {name}")
+
+
+@pytest.mark.parametrize("part", [64, 256])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_fused_step_split(monkeypatch, part, dtype):
+    monkeypatch.setenv("WLLM_PARTITION_TOKENS", str(part))
+    lens = [1, 63, 64, 65, 500, 1000, 2049, 0, 3000]
+    case = workloads.custom_case("fsplit", lens=lens, num_q_heads=28, num_kv_heads=4, head_dim=128,
+                                 block_size=16, dtype=dtype, seed=part + 5, heavy_key_frac=0.02)
+    got, _, _ = fused_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, dtype, f"fused split {part}")
+    got2, _, _ = fused_step(case)  # scheduler and barrier words left clean
+    assert torch.equal(int_view(got), int_view(got2))
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,bs", [SHAPES[0], SHAPES[4], SHAPES[8], SHAPES[12], SHAPES[15]])
+def test_fused_step_shapes(dtype, Hq, Hkv, D, bs):
+    case = workloads.custom_case("fshape", lens=LENS, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                                 block_size=bs, dtype=dtype, seed=Hq + D + bs + 1, spare_blocks=2)
+    got, kc, vc = fused_step(case)
+    ref, kr, vr = oracle_step(case)
+    assert torch.equal(int_view(kc.cpu()), int_view(kr))
+    assert_attention_close(got, ref, dtype, f"fused {dtype} {Hq}/{Hkv} D{D} bs{bs}")
+
+
+def test_separate_combine_kernel(monkeypatch):
+    monkeypatch.setenv("WLLM_SEPARATE_COMBINE", "1")
+    monkeypatch.setenv("WLLM_PARTITION_TOKENS", "128")
+    case = workloads.custom_case("sep", lens=[5, 900, 2500, 1], num_q_heads=8, num_kv_heads=2,
+                                 head_dim=64, block_size=16, dtype=torch.float16, seed=44)
+    got, _, _ = gpu_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, case.dtype, "separate combine")
+    got2, _, _ = fused_step(case)
+    assert_attention_close(got2, ref, case.dtype, "separate combine, step")
+
+
+def test_fused_step_without_tokens_or_sequences():
+    case = workloads.custom_case("noapp", lens=[40, 17], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                                 block_size=16, dtype=torch.bfloat16, seed=45, append="none")
+    got, _, _ = fused_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, case.dtype, "no append")
+    # attention over nothing, append only
+    kc = torch.zeros(2, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
+    vc = kc.clone()
+    key = torch.ones(1, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(0, 1, 64, dtype=torch.bfloat16, device="cuda")
+    wllm.decode_step(torch.empty_like(q), q, key, key, kc, vc, torch.tensor([17], device="cuda"),
+                     torch.zeros(0, 2, dtype=torch.int32, device="cuda"),
+                     torch.zeros(0, dtype=torch.int32, device="cuda"), 1, 0.1, 16)
+    torch.cuda.synchronize()
+    assert kc[1, 0, 1].float().sum().item() == 64

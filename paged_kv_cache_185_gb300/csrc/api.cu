@@ -689,6 +689,7 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = s->err;
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
+    p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 0) != 0;
     if (!pl.persistent && a.hkv * pl.tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
     if ((rc = bind_workspace(s, pl, st, p))) return rc;
     cudaError_t e;
@@ -908,6 +909,7 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = reinterpret_cast<int*>(scratch);
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
+    p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 0) != 0;
     p.ws_count = nullptr;
     p.ws_ml = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes) : nullptr;
     p.ws_o = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes + pl.ml_bytes) : nullptr;

@@ -79,9 +79,14 @@ __device__ __forceinline__ bool grid_barrier(int* ctrl, uint64_t limit_ns) {
 struct StageMeta {
   int b, p, t0, tok_end;
   int n_parts, h0, nh, flags;
-  int z, nsub, pad0, pad1;
+  int z, nsub, group, pad1;
 };
-enum : int { kFirst = 1, kLast = 2, kEmptySeq = 4, kStop = 8 };
+enum : int { kFirst = 1, kLast = 2, kEmptySeq = 4, kStop = 8, kGroup = 16 };
+
+// Consecutive sequences whose tables name the same physical blocks for a whole
+// partition (a shared prompt prefix) are processed as one unit of up to
+// kMaxGroup sequences: the K/V bytes are read once for all of them.
+constexpr int kMaxGroup = 8;
 
 constexpr int kSub = 4;                      // 16-token sub-chunks per stage
 constexpr int kStageTokens = kSub * kChunk;  // 64 tokens per stage
@@ -202,8 +207,171 @@ __device__ __forceinline__ void combine_row(const DecodeParams& p, int row, int 
   for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
 }
 
+// One 64-token stage for one sequence of a prefix group: four independent
+// 16-token S^T tiles (interleaved: four mma chains in flight), one online
+// softmax update over the stage, PV over the full head_dim.
+template <typename T, int D>
+__device__ __forceinline__ void mma_stage4(MmaState<T, D, 1>& st, uint32_t k_base, uint32_t v_base, int t0,
+                                           int tok_end, int nsub, float scale_log2, int lane) {
+  constexpr int kKV = Geom<T, D>::kTileBytes;
+  float s[kSub][4];
+#pragma unroll
+  for (int j = 0; j < kSub; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[j][i] = 0.f;
+  const int a_row = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int a_chunk = lane >> 4;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) {
+      if (j < nsub) {
+        uint32_t a[4];
+        ldsm_x4(k_base + j * kKV + tile_offset(a_row, 2 * ks + a_chunk), a);
+        Mma<T>::run(s[j], a, st.qb[0][ks]);
+      }
+    }
+  }
+  float x[kSub][4];
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kSub; ++j) {
+    const int tok_a = t0 + j * kChunk + (lane >> 2);
+    const bool va = tok_a < tok_end, vb = tok_a + 8 < tok_end;
+    x[j][0] = va ? s[j][0] * scale_log2 : -INFINITY;
+    x[j][1] = va ? s[j][1] * scale_log2 : -INFINITY;
+    x[j][2] = vb ? s[j][2] * scale_log2 : -INFINITY;
+    x[j][3] = vb ? s[j][3] * scale_log2 : -INFINITY;
+    mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
+    mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m[0][0], mx0), mn1 = fmaxf(st.m[0][1], mx1);
+  const float alpha0 = exp2f(st.m[0][0] - mn0), alpha1 = exp2f(st.m[0][1] - mn1);
+  st.m[0][0] = mn0;
+  st.m[0][1] = mn1;
+  uint32_t pb[kSub][2];
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kSub; ++j) {
+    const float p0 = exp2f(x[j][0] - mn0), p1 = exp2f(x[j][1] - mn1);
+    const float p2 = exp2f(x[j][2] - mn0), p3 = exp2f(x[j][3] - mn1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    pb[j][0] = movmatrix_trans(Mma<T>::pack(p0, p1));
+    pb[j][1] = movmatrix_trans(Mma<T>::pack(p2, p3));
+  }
+  st.l[0][0] = st.l[0][0] * alpha0 + l0;
+  st.l[0][1] = st.l[0][1] * alpha1 + l1;
+  if (__any_sync(kFullMask, (alpha0 != 1.f) || (alpha1 != 1.f))) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0][0] *= alpha0;
+      st.o[mt][0][1] *= alpha1;
+      st.o[mt][0][2] *= alpha0;
+      st.o[mt][0][3] *= alpha1;
+    }
+  }
+  const int v_row = (lane & 7) + ((lane >> 4) << 3);
+  const int v_chunk = (lane >> 3) & 1;
+#pragma unroll
+  for (int j = 0; j < kSub; ++j) {
+    if (j < nsub) {
+      const int tj = t0 + j * kChunk;
+      const bool tail = tj + kChunk > tok_end;
+      const int tk = tj + 2 * (lane & 3);
+      const uint32_t keep_lo = (tk < tok_end ? 0x0000ffffu : 0u) | (tk + 1 < tok_end ? 0xffff0000u : 0u);
+      const uint32_t keep_hi = (tk + 8 < tok_end ? 0x0000ffffu : 0u) | (tk + 9 < tok_end ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(v_base + j * kKV + tile_offset(v_row, 2 * mt + v_chunk), a);
+        if (tail) {
+          a[0] &= keep_lo;
+          a[1] &= keep_lo;
+          a[2] &= keep_hi;
+          a[3] &= keep_hi;
+        }
+        Mma<T>::run(st.o[mt][0], a, pb[j]);
+      }
+    }
+  }
+}
+
+// Query fragments of sequence b's heads h0.. from global memory (group units).
+template <typename T, int D>
+__device__ __forceinline__ void load_q_global(MmaState<T, D, 1>& st, const DecodeParams& p, int b, int h0, int nh,
+                                              int lane) {
+  const int hh = lane >> 2;
+  const bool valid = hh < nh;
+  const T* row = reinterpret_cast<const T*>(p.q) + b * p.q_sb + static_cast<int64_t>(h0 + (valid ? hh : 0)) * p.q_sh;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int d = ks * 16 + 2 * (lane & 3);
+    st.qb[0][ks][0] = valid ? *reinterpret_cast<const uint32_t*>(row + d) : 0u;
+    st.qb[0][ks][1] = valid ? *reinterpret_cast<const uint32_t*>(row + d + 8) : 0u;
+  }
+  st.m[0][0] = st.m[0][1] = -INFINITY;
+  st.l[0][0] = st.l[0][1] = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[mt][0][e] = 0.f;
+}
+
+// Finish one sequence of a prefix group (one warp holds all of it): the
+// output when the sequence has one partition, otherwise its partial.
+template <typename T, int D>
+__device__ __forceinline__ void finish_member(MmaState<T, D, 1>& st, const DecodeParams& p, int b, int part,
+                                              int h0, int nh, int lane) {
+  const int l_max = p.max_blocks * p.block_size;
+  int L = p.context_lens[b];
+  L = L < 0 ? 0 : (L > l_max ? l_max : L);
+  const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  float l[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float v = st.l[0][j];
+    v += __shfl_xor_sync(kFullMask, v, 4);
+    v += __shfl_xor_sync(kFullMask, v, 8);
+    v += __shfl_xor_sync(kFullMask, v, 16);
+    l[j] = v;
+  }
+  const int hh = 2 * (lane & 3);
+  T* out = reinterpret_cast<T*>(p.out);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (hh + j >= nh) continue;
+    if (n_parts == 1) {
+      const float inv = 1.f / l[j];
+      T* r = out + b * p.o_sb + static_cast<int64_t>(h0 + hh + j) * p.o_sh;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        const int d = mt * 16 + (lane >> 2);
+        r[d] = from_f32<T>(st.o[mt][0][j] * inv);
+        r[d + 8] = from_f32<T>(st.o[mt][0][2 + j] * inv);
+      }
+    } else {
+      const int64_t slot = static_cast<int64_t>(b * p.num_q_heads + h0 + hh + j) * p.max_parts + part;
+      float* wo = p.ws_o + slot * D;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        const int d = mt * 16 + (lane >> 2);
+        wo[d] = st.o[mt][0][j];
+        wo[d + 8] = st.o[mt][0][2 + j];
+      }
+      if ((lane >> 2) == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(st.m[0][j], l[j]);
+    }
+  }
+}
+
 struct UnitInfo {
   int b, part, z, n_parts, tb, te, n_chunks, kvh, h0, nh;
+  int group;  // sequences b .. b+group-1 share this partition (1: no sharing); 0: covered by a leader
 };
 
 template <typename T, int D, int NT>
@@ -215,6 +383,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   constexpr int S = PS::kStages;
   constexpr int W = PS::kConsumers;
   constexpr int HT = PS::kHeadTile;
+  constexpr bool kGroupOK = NT == 1 && D <= 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -294,6 +463,77 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         e1 = x1;
       }
     };
+    // Sharing of the full partition starting at token tb of sequence b with its
+    // neighbours: returns 0 when an earlier sequence's group covers b, else
+    // the number of sequences b.. (at most kMaxGroup) whose tables name the
+    // same physical blocks for the whole partition.  Block lists are compared
+    // a warp at a time (up to 64 blocks: two per lane); rows are loaded in
+    // batches (b-1..b+1 first, the rest only when a neighbour shares) so the
+    // check costs one or two round trips.
+    auto prefix_group = [&](int b, int tb) -> int {
+      const int nblk = p.part_tokens >> p.log2_bs;
+      const int j0 = tb >> p.log2_bs;
+      constexpr int R = kMaxGroup - 1;  // rows each side
+      auto load_row = [&](int bb, int& v0, int& v1) {
+        v0 = -1;
+        v1 = -1;
+        if (bb >= 0 && bb < B) {
+          const int32_t* r = p.block_tables + static_cast<int64_t>(bb) * p.bt_stride + j0;
+          if (lane < nblk) v0 = r[lane];
+          if (lane + 32 < nblk) v1 = r[lane + 32];
+        }
+      };
+      // lane i < 2R+1 holds whether row b-R+i fills the partition
+      auto covers_mask = [&]() -> unsigned {
+        const int bb = b - R + lane;
+        bool c = false;
+        if (lane < 2 * R + 1 && bb >= 0 && bb < B) {
+          int Lb = p.context_lens[bb];
+          Lb = Lb < 0 ? 0 : (Lb > l_max ? l_max : Lb);
+          c = Lb >= tb + p.part_tokens;
+        }
+        return __ballot_sync(kFullMask, c);
+      };
+      int c0, c1, a0, a1, n0, n1;
+      load_row(b, c0, c1);
+      load_row(b - 1, a0, a1);
+      load_row(b + 1, n0, n1);
+      const unsigned cov = covers_mask();
+      const bool prev = b > 0 && ((cov >> (R - 1)) & 1) && __all_sync(kFullMask, a0 == c0 && a1 == c1);
+      const bool next = b + 1 < B && ((cov >> (R + 1)) & 1) && __all_sync(kFullMask, n0 == c0 && n1 == c1);
+      if (!prev && !next) return 1;
+      int r0[2 * R + 1], r1[2 * R + 1];
+#pragma unroll
+      for (int i = 0; i < 2 * R + 1; ++i) load_row(b - R + i, r0[i], r1[i]);
+      unsigned same = 0;  // bit i: row b-R+i names the same blocks and fills the partition
+#pragma unroll
+      for (int i = 0; i < 2 * R + 1; ++i)
+        if (__all_sync(kFullMask, r0[i] == c0 && r1[i] == c1) && ((cov >> i) & 1)) same |= 1u << i;
+      int k = 0;  // sharing predecessors in a row
+      while (k < R && ((same >> (R - 1 - k)) & 1)) ++k;
+      if (k > 0) {
+        // the run's first sequence leads a group of up to kMaxGroup; so does
+        // every kMaxGroup-th one after it (a run longer than R back is
+        // rechecked from further back only in that rare case)
+        int run = k;
+        if (k == R) {
+          int bb = b - R - 1;
+          while (bb >= 0 && run % kMaxGroup != 0) {
+            int x0, x1;
+            load_row(bb, x0, x1);
+            int Lb = p.context_lens[bb];
+            Lb = Lb < 0 ? 0 : (Lb > l_max ? l_max : Lb);
+            if (!(__all_sync(kFullMask, x0 == c0 && x1 == c1) && Lb >= tb + p.part_tokens)) break;
+            ++run;
+            --bb;
+          }
+        }
+        if (run % kMaxGroup != 0) return 0;
+      }
+      int g = 1;
+      while (g < kMaxGroup && ((same >> (R + g)) & 1)) ++g;
+      return g;
+    };
     bool have_prefix = false;
     bool wait_ok = true;
     // unit u -> (sequence, partition, kv-head tile) and the table entries of
@@ -355,6 +595,12 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
       x.kvh = x.z / p.num_head_tiles;
       x.h0 = x.kvh * p.group + (x.z - x.kvh * p.num_head_tiles) * HT;
       x.nh = min(HT, p.group - (x.z - x.kvh * p.num_head_tiles) * HT);
+      x.group = 1;
+      if constexpr (kGroupOK) {
+        if (p.prefix_groups && L >= x.tb + p.part_tokens && (p.part_tokens & (p.block_size - 1)) == 0 &&
+            (p.part_tokens >> p.log2_bs) <= 64)
+          x.group = prefix_group(x.b, x.tb);
+      }
       return true;
     };
     int k = 0;  // stage sequence number
@@ -390,7 +636,9 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         if (have_nxt && lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
         fetched = true;
       };
-      if (cur.n_chunks == 0) {
+      if (cur.group == 0) {
+        // covered by its group's leader: nothing to issue
+      } else if (cur.n_chunks == 0) {
         if (!acquire_stage(k)) { ok = false; break; }
         if (lane == 0) {
           meta[k % S] = StageMeta{cur.b, cur.part, 0, 0, cur.n_parts, cur.h0, cur.nh,
@@ -418,8 +666,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
             const int nsub = min(kSub, cur.n_chunks - c0);
             const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
             const uint32_t bar = smem_u32(full + s);
-            const int flags = (sg == 0 ? kFirst : 0) | (sg == n_stages - 1 ? kLast : 0);
-            meta[s] = StageMeta{cur.b, cur.part, t0, cur.te, cur.n_parts, cur.h0, cur.nh, flags, cur.z, nsub, 0, 0};
+            const int flags =
+                (sg == 0 ? kFirst : 0) | (sg == n_stages - 1 ? kLast : 0) | (cur.group > 1 ? kGroup : 0);
+            meta[s] = StageMeta{cur.b, cur.part, t0, cur.te, cur.n_parts, cur.h0, cur.nh, flags, cur.z, nsub,
+                                cur.group, 0};
             const bool two = p.log2_bs < 4;
             uint32_t bytes = 0;
 #pragma unroll
@@ -429,7 +679,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
                 bytes += (two && !(tj + 8 < cur.te)) ? G::kStageBytes / 2 : G::kStageBytes;
               }
             }
-            if (sg == 0) bytes += cur.nh * D * static_cast<int>(sizeof(T));
+            const bool q_rows = sg == 0 && cur.group == 1;  // group units read q from global memory
+            if (q_rows) bytes += cur.nh * D * static_cast<int>(sizeof(T));
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
             for (int j = 0; j < kSub; ++j) {
@@ -459,7 +710,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
                 }
               }
             }
-            if (sg == 0) {
+            if (q_rows) {
               for (int hh = 0; hh < cur.nh; ++hh)
                 bulk_load(stage + 2 * kSub * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
                           D * static_cast<int>(sizeof(T)), bar);
@@ -533,6 +784,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   }
   if ((flags & kFuseAppend) && !cta_grid_sync()) failed = true;
   MmaState<T, D, NT> st;
+  MmaState<T, D, 1> st2;  // second sequence of a prefix group (group units only)
   const int cw = warp;
   float* red_o = reinterpret_cast<float*>(red_area);  // [W][HT][D]
   float* red_m = red_o + W * HT * D;                  // [W][HT]
@@ -550,6 +802,26 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     const StageMeta mt_ = meta[s];
     if (mt_.flags & kStop) break;
     const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
+    if constexpr (kGroupOK) {
+      if (mt_.flags & kGroup) {  // warp cw takes sequences b+cw and b+cw+4 of the group, all 64 tokens
+        const bool has0 = cw < mt_.group, has1 = cw + W < mt_.group;
+        if (mt_.flags & kFirst) {
+          if (has0) load_q_global<T, D>(st, p, mt_.b + cw, mt_.h0, mt_.nh, lane);
+          if (has1) load_q_global<T, D>(st2, p, mt_.b + cw + W, mt_.h0, mt_.nh, lane);
+        }
+        if (has0)
+          mma_stage4<T, D>(st, stage, stage + kSub * PS::kKV, mt_.t0, mt_.tok_end, mt_.nsub, p.scale_log2, lane);
+        if (has1)
+          mma_stage4<T, D>(st2, stage, stage + kSub * PS::kKV, mt_.t0, mt_.tok_end, mt_.nsub, p.scale_log2, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        if (mt_.flags & kLast) {
+          if (has0) finish_member<T, D>(st, p, mt_.b + cw, mt_.p, mt_.h0, mt_.nh, lane);
+          if (has1) finish_member<T, D>(st2, p, mt_.b + cw + W, mt_.p, mt_.h0, mt_.nh, lane);
+        }
+        continue;
+      }
+    }
     if (!(mt_.flags & kEmptySeq)) {
       if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, ring + s * PS::kStageBytes + 2 * kSub * PS::kKV, mt_.nh, lane);
       if (cw < mt_.nsub)

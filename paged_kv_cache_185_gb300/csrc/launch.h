@@ -27,6 +27,7 @@ struct DecodeParams {
   int* ws_count;                  // [B*Hkv*num_head_tiles] arrival counters, zero between calls
   int* err;                       // device error word
   unsigned long long wait_limit_ns;
+  int prefix_groups;              // process shared-prefix partitions once per group of sequences
 };
 
 struct AppendParams {

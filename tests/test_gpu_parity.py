@@ -461,3 +461,29 @@ def test_fused_step_without_tokens_or_sequences():
                      torch.zeros(0, dtype=torch.int32, device="cuda"), 1, 0.1, 16)
     torch.cuda.synchronize()
     assert kc[1, 0, 1].float().sum().item() == 64
+
+
+# ---------------------------------------------------------------------------
+# prefix groups: sequences sharing a partition's blocks are processed once
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gsize,shared,part", [(8, 64, 512), (12, 40, 128), (3, 33, 256), (5, 16, 256),
+                                               (1, 20, 128), (9, 8, 128)])
+@pytest.mark.parametrize("dtype,Hq,Hkv,D", [(torch.bfloat16, 28, 4, 128), (torch.float16, 16, 4, 64)])
+def test_prefix_groups(monkeypatch, gsize, shared, part, dtype, Hq, Hkv, D):
+    monkeypatch.setenv("WLLM_PARTITION_TOKENS", str(part))
+    monkeypatch.setenv("WLLM_PREFIX_GROUPS", "1")
+    g = torch.Generator().manual_seed(gsize * 100 + shared)
+    n_groups = 3
+    lens = [shared * 16 + int(x) for x in torch.randint(1, 700, (gsize * n_groups,), generator=g)]
+    lens[0] = shared * 16 + 1  # a member whose only private token is the appended one
+    case = workloads.custom_case("groups", lens=lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                                 block_size=16, dtype=dtype, seed=gsize + shared, groups=(gsize, shared))
+    got, _, _ = gpu_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, dtype, f"groups {gsize}x{shared} P{part}")
+    got_f, _, _ = fused_step(case)
+    assert_attention_close(got_f, ref, dtype, f"groups fused {gsize}x{shared} P{part}")
+    monkeypatch.setenv("WLLM_PREFIX_GROUPS", "0")
+    got0, _, _ = gpu_step(case)
+    assert_attention_close(got0, ref, dtype, "groups off")

@@ -91,29 +91,60 @@ constexpr int kMaxGroup = 8;
 constexpr int kSub = 4;                      // 16-token sub-chunks per stage
 constexpr int kStageTokens = kSub * kChunk;  // 64 tokens per stage
 
+// One unit of work: query heads h0 .. h0+nh-1 (kv head kvh, head tile z) of
+// sequence b over tokens [tb, te) of partition `part`.
+struct UnitInfo {
+  int b, part, z, n_parts, tb, te, n_chunks, kvh, h0, nh;
+  int group;  // sequences b .. b+group-1 share this partition (1: no sharing); 0: covered by a leader
+};
+
+// A piece of a unit handed from the scheduler warp to the producer warp: the
+// block-table entries of up to kPieceChunks 16-token chunks starting at chunk
+// c0 of the unit (two entries per chunk when blocks hold 8 tokens).
+constexpr int kPieceChunks = 32;
+constexpr int kQueue = 4;  // pieces in flight between scheduler and producer
+enum : int { kPieceFirst = 1, kPieceLast = 2, kPieceStop = 4 };
+struct Piece {
+  UnitInfo u;
+  int c0, flags, pad0, pad1, pad2;
+  int e[2 * kPieceChunks];
+};
+static_assert(sizeof(Piece) % 16 == 0, "pieces stay 16-byte aligned");
+
 template <typename T, int D, int NT>
 struct PShape {
   static constexpr int kConsumers = 4;
-  static constexpr int kThreads = (kConsumers + 1) * 32;
+  static constexpr int kThreads = (kConsumers + 2) * 32;  // consumers, producer, scheduler
   static constexpr int kHeadTile = 8 * NT;
   static constexpr int kKV = Geom<T, D>::kTileBytes;  // one 16-row K (or V) sub-tile
   static constexpr int kQBytes = kHeadTile * D * static_cast<int>(sizeof(T));
   static constexpr int kStageBytes = ((2 * kSub * kKV + kQBytes) + 1023) / 1024 * 1024;
+  // the unit merge writes each consumer's (m, l, O) into the ring slot of
+  // the unit's last stage once every consumer is done reading it
   static constexpr int kRedBytes = (kConsumers * kHeadTile * (D + 2) * 4 + 127) / 128 * 128;
-  // Consumer warps, not ring depth, bound the rate (each 16-token sub-chunk is
-  // a ~1-2k-cycle dependency chain), so the target is two or three CTAs per
-  // SM (eight or more consumer warps); the ring gets what is left of the
-  // per-CTA share of shared memory after the reduction area, the
-  // per-sequence arrays (up to kPersistentMaxSeqs) and the barriers.
+  static_assert(kRedBytes <= kStageBytes, "unit merge must fit in one ring slot");
+  // Consumer warps bound the rate of one CTA (each 16-token sub-chunk is a
+  // ~1k-cycle dependency chain), so the target is two or three CTAs per SM
+  // (eight or more consumer warps).  The ring gets what is left of the
+  // per-CTA share of shared memory (228 KB per SM, 1 KB of it reserved per
+  // CTA) after the alignment pad, the barriers and stage records (64 B per
+  // stage), the piece queue and the prefix-sum array (up to
+  // kPersistentMaxSeqs + 1 ints).
   static constexpr int kCtasPerSm = D == 64 ? 3 : (D == 128 ? 2 : 1);
-  static constexpr int kSmemBudget =
-      227 * 1024 / kCtasPerSm - 1024 - 1024 - kRedBytes - (2 * kPersistentMaxSeqs + 1) * 4 - 2048;
-  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
+  // registers per thread that keep kCtasPerSm CTAs resident (64K per SM, a
+  // multiple of 8 per thread)
+  static constexpr int kMaxRegsRaw = 65536 / (kCtasPerSm * kThreads) / 8 * 8;
+  static constexpr int kMaxRegs = kMaxRegsRaw > 255 ? 255 : kMaxRegsRaw;
+  static constexpr int kSeqBytes = ((kPersistentMaxSeqs + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kSmemPerCta = 233472 / kCtasPerSm - 1024;
+  static constexpr int kQueueBytes = kQueue * (static_cast<int>(sizeof(Piece)) + 16);
+  static constexpr int kStagesRaw = (kSmemPerCta - 1024 - 64 - 16 - kSeqBytes - kQueueBytes) / (kStageBytes + 64);
   static constexpr int kStages = kStagesRaw > 16 ? 16 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kBarBytes = (2 * kStages + 2) * 8;
+  static constexpr int kBarBytes = (2 * kStages + 2 + 2 * kQueue) * 8;
   static constexpr int kMetaBytes = kStages * static_cast<int>(sizeof(StageMeta));
-  static constexpr int kFixedSmem = 1024 + kRingBytes + kRedBytes + kBarBytes + kMetaBytes + 64;
+  static constexpr int kFixedSmem =
+      1024 + kRingBytes + kBarBytes + kMetaBytes + kQueue * static_cast<int>(sizeof(Piece)) + 64;
 };
 
 // Query fragments of a unit from the stage's query rows (row stride D).
@@ -369,13 +400,8 @@ __device__ __forceinline__ void finish_member(MmaState<T, D, 1>& st, const Decod
   }
 }
 
-struct UnitInfo {
-  int b, part, z, n_parts, tb, te, n_chunks, kvh, h0, nh;
-  int group;  // sequences b .. b+group-1 share this partition (1: no sharing); 0: covered by a leader
-};
-
 template <typename T, int D, int NT>
-__global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
+__global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShape<T, D, NT>::kMaxRegs))
     paged_decode_persistent(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                             const DecodeParams p, const AppendParams ap, const int flags) {
   using G = Geom<T, D>;
@@ -383,20 +409,22 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   constexpr int S = PS::kStages;
   constexpr int W = PS::kConsumers;
   constexpr int HT = PS::kHeadTile;
+  constexpr int Q = kQueue;
   constexpr bool kGroupOK = NT == 1 && D <= 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* red_area = smem + PS::kRingBytes;  // consumers' (m, l, O) for the unit merge
-  uint64_t* full = reinterpret_cast<uint64_t*>(red_area + PS::kRedBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PS::kRingBytes);
   uint64_t* empty = full + S;
   uint64_t* cbar = empty + S;                 // consumer rendezvous
-  uint64_t* pbar = cbar + 1;                  // prefix sums ready (consumers -> producer)
-  StageMeta* meta = reinterpret_cast<StageMeta*>(pbar + 1);
-  int* wsum = reinterpret_cast<int*>(meta + S);  // 16 ints of scratch
+  uint64_t* pbar = cbar + 1;                  // prefix sums ready (consumers -> scheduler)
+  uint64_t* qfull = pbar + 1;                 // piece queue: scheduler -> producer
+  uint64_t* qempty = qfull + kQueue;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(qempty + kQueue);
+  Piece* pieces = reinterpret_cast<Piece*>(meta + S);
+  int* wsum = reinterpret_cast<int*>(pieces + kQueue);  // 16 ints of scratch
   int* prefix = wsum + 16;                       // [B + 1] units before sequence b
-  int* lens = prefix + p.num_seqs + 1;           // [B] clamped context lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.num_seqs;
@@ -410,6 +438,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     }
     mbar_init(smem_u32(cbar), W);
     mbar_init(smem_u32(pbar), 1);
+    for (int i = 0; i < Q; ++i) {
+      mbar_init(smem_u32(qfull + i), 1);
+      mbar_init(smem_u32(qempty + i), 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -419,8 +451,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   // CTAs' tensor copies before any of them reads the cache (grid barrier below)
   if (flags & kFuseAppend) {
     const int64_t rows = static_cast<int64_t>(ap.num_tokens) * ap.num_kv_heads;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (W + 1) + warp; r < rows;
-         r += static_cast<int64_t>(gridDim.x) * (W + 1))
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (W + 2) + warp; r < rows;
+         r += static_cast<int64_t>(gridDim.x) * (W + 2))
       append_row(ap, r, lane);
     asm volatile("fence.proxy.async.global;" ::: "memory");
   }
@@ -435,12 +467,14 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     return ok_;
   };
 
-  if (warp == W) {
-    // ------------------------------- producer -------------------------------
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
+  if (warp == W + 1) {
+    // ------------------------------- scheduler -------------------------------
+    // Claims units (CTA i starts with unit i; later ones come from the global
+    // counter, offset by the grid size), decodes them, loads their block-table
+    // entries and hands them to the producer as pieces of at most kPieceChunks
+    // chunks through a kQueue-deep queue in shared memory.  Every
+    // global-memory round trip of the schedule happens here, off the path
+    // between two tensor-copy issues.
     int* sched_next = p.err + kSchedNextOffset;
     int* sched_done = p.err + kSchedDoneOffset;
 
@@ -585,7 +619,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         const int r = u2 - prefix[lo];
         x.part = 1 + r / Z;
         x.z = r - (r / Z) * Z;
-        L = lens[lo];
+        L = p.context_lens[lo];  // checked and clamped by the consumers' prefix pass
+        L = L < 0 ? 0 : (L > l_max ? l_max : L);
         x.tb = x.part * p.part_tokens;
         x.te = min(L, x.tb + p.part_tokens);
         x.n_chunks = (x.te - x.tb + kChunk - 1) / kChunk;
@@ -603,43 +638,104 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
       }
       return true;
     };
-    int k = 0;  // stage sequence number
     bool ok = true;
+    int pk = 0;  // pieces handed over
+    auto put_piece = [&](const UnitInfo& x, int c0, int pflags, int e0, int e1) -> bool {
+      bool got = true;
+      if (lane == 0) got = mbar_wait_bounded(smem_u32(qempty + pk % Q), ((pk / Q) & 1) ^ 1, p.wait_limit_ns);
+      if (__shfl_sync(kFullMask, got ? 1 : 0, 0) == 0) return false;
+      Piece& pc = pieces[pk % Q];
+      if (lane == 0) {
+        pc.u = x;
+        pc.c0 = c0;
+        pc.flags = pflags;
+      }
+      pc.e[2 * lane] = e0;
+      pc.e[2 * lane + 1] = e1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(qfull + pk % Q));
+      ++pk;
+      return true;
+    };
+    UnitInfo cur{};
+    int e0 = 0, e1 = 0;
+    bool have_cur = decode_unit(static_cast<int>(blockIdx.x), cur, e0, e1);
+    int raw_next = 0;  // the next unit id is always requested one unit ahead
+    if (lane == 0 && have_cur) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+    if (flags & kFuseAppend) {
+      if (!cta_grid_sync()) ok = false;
+    }
+    while (ok && have_cur) {
+      if (cur.group == 0) {
+        // covered by its group's leader: nothing to hand over
+      } else if (cur.n_chunks == 0) {
+        ok = put_piece(cur, 0, kPieceFirst | kPieceLast, 0, 0);
+      } else {
+        for (int c0 = 0; ok && c0 < cur.n_chunks; c0 += kPieceChunks) {
+          if (c0 > 0) load_entries(cur, c0, e0, e1);
+          ok = put_piece(cur, c0, (c0 == 0 ? kPieceFirst : 0) | (c0 + kPieceChunks >= cur.n_chunks ? kPieceLast : 0),
+                         e0, e1);
+        }
+      }
+      if (!ok) break;
+      const int u_nxt = __shfl_sync(kFullMask, raw_next, 0);
+      have_cur = decode_unit(u_nxt, cur, e0, e1);
+      if (!wait_ok) {
+        ok = false;
+        break;
+      }
+      if (have_cur && lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+    }
+    if (!put_piece(UnitInfo{}, 0, kPieceStop, 0, 0)) ok = false;
+    if (!ok && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+    if (lane == 0) {  // the last CTA to finish leaves the counters at zero for the next launch
+      __threadfence();
+      if (atomicAdd(sched_done, 1) == static_cast<int>(gridDim.x) - 1) {
+        atomicExch(sched_next, 0);
+        atomicExch(sched_done, 0);
+      }
+    }
+    failed = !ok;
+  } else if (warp == W) {
+    // ------------------------------- producer -------------------------------
+    // Turns queued pieces into 64-token stages: waits for a free ring slot,
+    // records the stage, and issues its tensor copies (plus the unit's query
+    // rows with its first stage).
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+    }
+    if (flags & kFuseAppend) {  // no cache read before every CTA's append is done
+      if (!cta_grid_sync()) failed = true;
+    }
+    int k = 0;   // stage sequence number
+    int pk = 0;  // pieces taken
+    bool ok = !failed;
     auto acquire_stage = [&](int kk) -> bool {
       bool got = true;
       if (lane == 0) got = mbar_wait_bounded(smem_u32(empty + kk % S), ((kk / S) & 1) ^ 1, p.wait_limit_ns);
       return __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
     };
-
-    // the unit being issued, the next one (entries prefetched), and the id
-    // after that (its atomic still in flight)
-    // the first unit of CTA i is unit i; later ones come from the counter
-    // (offset by the grid size); the next id is always requested one unit
-    // ahead so its latency hides behind the current unit's copies
-    UnitInfo cur{};
-    int e0 = 0, e1 = 0;
-    bool have_cur = decode_unit(static_cast<int>(blockIdx.x), cur, e0, e1);
-    int raw_next = 0;
-    if (lane == 0 && have_cur) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
-    if (flags & kFuseAppend) {  // no cache read before every CTA's append is done
-      if (!cta_grid_sync()) ok = false;
-    }
-    while (ok && have_cur) {
-      // the next unit is fetched once the current one has filled the ring
-      // (or has no more stages), so its latency overlaps the copies in flight
-      UnitInfo nxt{};
-      int f0 = 0, f1 = 0;
-      bool have_nxt = false, fetched = false;
-      auto fetch_next = [&]() {
-        const int u_nxt = __shfl_sync(kFullMask, raw_next, 0);
-        have_nxt = decode_unit(u_nxt, nxt, f0, f1);
-        if (have_nxt && lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
-        fetched = true;
-      };
-      if (cur.group == 0) {
-        // covered by its group's leader: nothing to issue
-      } else if (cur.n_chunks == 0) {
-        if (!acquire_stage(k)) { ok = false; break; }
+    while (ok) {
+      bool got = true;
+      if (lane == 0) got = mbar_wait_bounded(smem_u32(qfull + pk % Q), (pk / Q) & 1, p.wait_limit_ns);
+      if (__shfl_sync(kFullMask, got ? 1 : 0, 0) == 0) {
+        ok = false;
+        break;
+      }
+      const Piece& pc = pieces[pk % Q];
+      const UnitInfo cur = pc.u;
+      const int pc0 = pc.c0, pflags = pc.flags;
+      const int e0 = pc.e[2 * lane], e1 = pc.e[2 * lane + 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(qempty + pk % Q));  // the piece is copied out: slot free
+      ++pk;
+      if (pflags & kPieceStop) break;
+      if (cur.n_chunks == 0) {
+        if (!acquire_stage(k)) {
+          ok = false;
+          break;
+        }
         if (lane == 0) {
           meta[k % S] = StageMeta{cur.b, cur.part, 0, 0, cur.n_parts, cur.h0, cur.nh,
                                   kFirst | kLast | kEmptySeq, cur.z, 0, 0, 0};
@@ -648,16 +744,15 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         ++k;
       } else {
         const T* qsrc = reinterpret_cast<const T*>(p.q) + cur.b * p.q_sb + static_cast<int64_t>(cur.h0) * p.q_sh;
-        const int n_stages = (cur.n_chunks + kSub - 1) / kSub;
-        const int fetch_after = (n_stages < S ? n_stages : S) - 1;
+        const int piece_chunks = min(kPieceChunks, cur.n_chunks - pc0);
+        const int n_stages = (piece_chunks + kSub - 1) / kSub;
         for (int sg = 0; sg < n_stages; ++sg) {
-          const int c0 = sg * kSub;
-          if (c0 > 0 && (c0 & 31) == 0) load_entries(cur, c0, e0, e1);
+          const int c0 = pc0 + sg * kSub;
           int pbs0[kSub], pbs1[kSub];
 #pragma unroll
           for (int j = 0; j < kSub; ++j) {
-            pbs0[j] = __shfl_sync(kFullMask, e0, (c0 + j) & 31);
-            pbs1[j] = __shfl_sync(kFullMask, e1, (c0 + j) & 31);
+            pbs0[j] = __shfl_sync(kFullMask, e0, (sg * kSub + j) & 31);
+            pbs1[j] = __shfl_sync(kFullMask, e1, (sg * kSub + j) & 31);
           }
           if (!acquire_stage(k)) { ok = false; break; }
           if (lane == 0) {
@@ -666,8 +761,9 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
             const int nsub = min(kSub, cur.n_chunks - c0);
             const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
             const uint32_t bar = smem_u32(full + s);
-            const int flags =
-                (sg == 0 ? kFirst : 0) | (sg == n_stages - 1 ? kLast : 0) | (cur.group > 1 ? kGroup : 0);
+            const bool first = (pflags & kPieceFirst) && sg == 0;
+            const int flags = (first ? kFirst : 0) | ((pflags & kPieceLast) && sg == n_stages - 1 ? kLast : 0) |
+                              (cur.group > 1 ? kGroup : 0);
             meta[s] = StageMeta{cur.b, cur.part, t0, cur.te, cur.n_parts, cur.h0, cur.nh, flags, cur.z, nsub,
                                 cur.group, 0};
             const bool two = p.log2_bs < 4;
@@ -679,7 +775,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
                 bytes += (two && !(tj + 8 < cur.te)) ? G::kStageBytes / 2 : G::kStageBytes;
               }
             }
-            const bool q_rows = sg == 0 && cur.group == 1;  // group units read q from global memory
+            const bool q_rows = first && cur.group == 1;  // group units read q from global memory
             if (q_rows) bytes += cur.nh * D * static_cast<int>(sizeof(T));
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
@@ -717,36 +813,21 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
             }
           }
           ++k;
-          if (sg == fetch_after) fetch_next();
-          if (!wait_ok) { ok = false; break; }
         }
       }
-      if (!ok) break;
-      if (!fetched) fetch_next();
-      if (!wait_ok) { ok = false; break; }
-      cur = nxt;
-      e0 = f0;
-      e1 = f1;
-      have_cur = have_nxt;
     }
-    // tell the consumers to stop, then leave the scheduler clean
-    if (!wait_ok) ok = false;
+    // tell the consumers to stop
     if (ok && acquire_stage(k)) {
       if (lane == 0) {
         meta[k % S].flags = kStop;
         mbar_arrive_expect_tx(smem_u32(full + k % S), 0);
       }
-    } else if (lane == 0) {
-      atomicOr(p.err, kErrWaitTimeout);
-    }
-    if (lane == 0) {
-      __threadfence();
-      if (atomicAdd(sched_done, 1) == static_cast<int>(gridDim.x) - 1) {
-        atomicExch(sched_next, 0);
-        atomicExch(sched_done, 0);
-      }
+    } else {
+      ok = false;
+      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
     }
     failed = !ok;
+
   } else {
 
   // ------------------------------- consumers --------------------------------
@@ -760,7 +841,6 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     for (int b = lo; b < hi; ++b) {
       int L = p.context_lens[b];
       L = L < 0 ? 0 : (L > l_max ? l_max : L);
-      lens[b] = L;
       local += (L == 0 ? 0 : (L + p.part_tokens - 1) / p.part_tokens - 1) * Z;
     }
     int incl = local;
@@ -773,9 +853,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
     int run = incl - local;
     for (int w = 0; w < warp; ++w) run += wsum[w];
-    for (int b = lo; b < hi; ++b) {
+    for (int b = lo; b < hi; ++b) {  // second read of the same lengths: L1/L2 hits
       prefix[b] = run;
-      const int L = lens[b];
+      int L = p.context_lens[b];
+      L = L < 0 ? 0 : (L > l_max ? l_max : L);
       run += (L == 0 ? 0 : (L + p.part_tokens - 1) / p.part_tokens - 1) * Z;
     }
     if (threadIdx.x == kCT - 1) prefix[B] = wsum[0] + wsum[1] + wsum[2] + wsum[3];
@@ -786,9 +867,6 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   MmaState<T, D, NT> st;
   MmaState<T, D, 1> st2;  // second sequence of a prefix group (group units only)
   const int cw = warp;
-  float* red_o = reinterpret_cast<float*>(red_area);  // [W][HT][D]
-  float* red_m = red_o + W * HT * D;                  // [W][HT]
-  float* red_l = red_m + W * HT;                      // [W][HT]
   const uint32_t sync_bar = smem_u32(cbar);
   int sync_phase = 0;
   T* out = reinterpret_cast<T*>(p.out);
@@ -829,7 +907,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
                             mt_.tok_end, p.scale_log2, lane);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    // the slot of a unit's last stage is kept for the merge and released after it
+    if (!(mt_.flags & kLast) || (mt_.flags & kEmptySeq)) {
+      if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    }
     if (!(mt_.flags & kLast)) continue;
 
     // ---- the unit is complete: merge the four warps, write out or a partial
@@ -841,6 +922,15 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
       }
       continue;
     }
+    // every consumer is done reading the slot's K/V before any overwrites it
+    if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
+      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+      failed = true;
+      break;
+    }
+    float* red_o = reinterpret_cast<float*>(ring + s * PS::kStageBytes);  // [W][HT][D]
+    float* red_m = red_o + W * HT * D;                                      // [W][HT]
+    float* red_l = red_m + W * HT;                                          // [W][HT]
     mma_store<T, D, NT>(st, red_o + cw * HT * D, red_m + cw * HT, red_l + cw * HT, lane);
     if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
@@ -887,11 +977,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
         if (lane == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, den);
       }
     }
-    if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {  // reduction area free again
-      if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
-      failed = true;
-      break;
-    }
+    // this warp's merge-area accesses are done: order them before the tensor
+    // copies that will refill the slot, then release it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(empty + s));
   }
   }  // consumers
 
@@ -899,8 +989,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads)
   // merge the split rows (one warp per query row)
   if (flags & kFuseCombine) {
     if (cta_grid_sync() && !failed) {
-      const int gwarp = static_cast<int>(blockIdx.x) * (W + 1) + warp;
-      for (int row = gwarp; row < B * p.num_q_heads; row += static_cast<int>(gridDim.x) * (W + 1))
+      const int gwarp = static_cast<int>(blockIdx.x) * (W + 2) + warp;
+      for (int row = gwarp; row < B * p.num_q_heads; row += static_cast<int>(gridDim.x) * (W + 2))
         combine_row<T, D>(p, row, lane);
     }
   }
@@ -917,7 +1007,7 @@ __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
 
 template <typename T, int D, int NT>
 int persistent_smem(int num_seqs) {
-  return PShape<T, D, NT>::kFixedSmem + ((2 * num_seqs + 1) * 4 + 15) / 16 * 16;
+  return PShape<T, D, NT>::kFixedSmem + ((num_seqs + 1) * 4 + 15) / 16 * 16;
 }
 
 // Launch the persistent decode.  `ap` non-null fuses the KV append in front of

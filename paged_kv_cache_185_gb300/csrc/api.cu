@@ -340,6 +340,7 @@ DecodePlan make_plan(int dt, int64_t B, int64_t hq, int64_t hkv, int64_t d, int6
     const int occ = decode_persistent_occupancy(dt, static_cast<int>(d), pl.head_tile, static_cast<int>(B));
     const int64_t n_ctas = int64_t(num_sms > 0 ? num_sms : 148) * occ;
     pl.part_tokens = choose_partition_persistent(B, z, tokens_max, n_ctas);
+    while ((tokens_max + pl.part_tokens - 1) / pl.part_tokens > kPersistentMaxParts) pl.part_tokens *= 2;
     pl.max_parts = static_cast<int>((tokens_max + pl.part_tokens - 1) / pl.part_tokens);
     pl.grid = static_cast<int>(std::min<int64_t>(n_ctas, std::max<int64_t>(1, B * z * pl.max_parts)));
     pl.separate_combine = pl.max_parts > 1;

@@ -103,6 +103,9 @@ struct UnitInfo {
 // c0 of the unit (two entries per chunk when blocks hold 8 tokens).
 constexpr int kPieceChunks = 32;
 constexpr int kQueue = 4;  // pieces in flight between scheduler and producer
+// The scheduler claims another unit only when at most this much work (in
+// 64-token stage equivalents) waits in the queue.
+constexpr int kLookahead = 8;
 enum : int { kPieceFirst = 1, kPieceLast = 2, kPieceStop = 4 };
 struct Piece {
   UnitInfo u;
@@ -124,13 +127,15 @@ struct PShape {
   static constexpr int kRedBytes = (kConsumers * kHeadTile * (D + 2) * 4 + 127) / 128 * 128;
   static_assert(kRedBytes <= kStageBytes, "unit merge must fit in one ring slot");
   // Consumer warps bound the rate of one CTA (each 16-token sub-chunk is a
-  // ~1k-cycle dependency chain), so the target is two or three CTAs per SM
-  // (eight or more consumer warps).  The ring gets what is left of the
+  // ~1k-cycle dependency chain), so the target is two CTAs per SM (eight
+  // consumer warps); a third would need under 100 registers a thread (each
+  // SM sub-partition holds 16K registers and would host five of the 18
+  // warps).  The ring gets what is left of the
   // per-CTA share of shared memory (228 KB per SM, 1 KB of it reserved per
   // CTA) after the alignment pad, the barriers and stage records (64 B per
   // stage), the piece queue and the prefix-sum array (up to
   // kPersistentMaxSeqs + 1 ints).
-  static constexpr int kCtasPerSm = D == 64 ? 3 : (D == 128 ? 2 : 1);
+  static constexpr int kCtasPerSm = D <= 128 ? 2 : 1;
   // registers per thread that keep kCtasPerSm CTAs resident (64K per SM, a
   // multiple of 8 per thread)
   static constexpr int kMaxRegsRaw = 65536 / (kCtasPerSm * kThreads) / 8 * 8;
@@ -238,79 +243,87 @@ __device__ __forceinline__ void combine_row(const DecodeParams& p, int row, int 
   for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
 }
 
-// One 64-token stage for one sequence of a prefix group: four independent
-// 16-token S^T tiles (interleaved: four mma chains in flight), one online
-// softmax update over the stage, PV over the full head_dim.
-template <typename T, int D>
-__device__ __forceinline__ void mma_stage4(MmaState<T, D, 1>& st, uint32_t k_base, uint32_t v_base, int t0,
-                                           int tok_end, int nsub, float scale_log2, int lane) {
+// NS consecutive 16-token sub-chunks (sub-chunk j's K at k_base + j * kKV,
+// its V at v_base + j * kKV; the first nsub hold tokens) for the NT column
+// tiles of `st`: NS x NT independent S^T tiles in flight, one online-softmax
+// update per column tile over all NS sub-chunks, then PV over the full
+// head_dim.  Used by prefix-group units, where each column tile is one
+// member sequence.  The first sub-chunk must hold at least one token.
+template <typename T, int D, int NT, int NS>
+__device__ __forceinline__ void mma_multi(MmaState<T, D, NT>& st, uint32_t k_base, uint32_t v_base, int t0,
+                                          int tok_end, int nsub, float scale_log2, int lane) {
   constexpr int kKV = Geom<T, D>::kTileBytes;
-  float s[kSub][4];
+  float s[NS][NT][4];
 #pragma unroll
-  for (int j = 0; j < kSub; ++j)
+  for (int j = 0; j < NS; ++j)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[j][i] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[j][nt][i] = 0.f;
   const int a_row = (lane & 7) + (((lane >> 3) & 1) << 3);
   const int a_chunk = lane >> 4;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-    for (int j = 0; j < kSub; ++j) {
+    for (int j = 0; j < NS; ++j) {
       if (j < nsub) {
         uint32_t a[4];
         ldsm_x4(k_base + j * kKV + tile_offset(a_row, 2 * ks + a_chunk), a);
-        Mma<T>::run(s[j], a, st.qb[0][ks]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) Mma<T>::run(s[j][nt], a, st.qb[nt][ks]);
       }
     }
   }
-  float x[kSub][4];
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  uint32_t pb[NS][NT][2];
 #pragma unroll
-  for (int j = 0; j < kSub; ++j) {
-    const int tok_a = t0 + j * kChunk + (lane >> 2);
-    const bool va = tok_a < tok_end, vb = tok_a + 8 < tok_end;
-    x[j][0] = va ? s[j][0] * scale_log2 : -INFINITY;
-    x[j][1] = va ? s[j][1] * scale_log2 : -INFINITY;
-    x[j][2] = vb ? s[j][2] * scale_log2 : -INFINITY;
-    x[j][3] = vb ? s[j][3] * scale_log2 : -INFINITY;
-    mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
-    mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
-  }
+  for (int nt = 0; nt < NT; ++nt) {
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
-  }
-  const float mn0 = fmaxf(st.m[0][0], mx0), mn1 = fmaxf(st.m[0][1], mx1);
-  const float alpha0 = exp2f(st.m[0][0] - mn0), alpha1 = exp2f(st.m[0][1] - mn1);
-  st.m[0][0] = mn0;
-  st.m[0][1] = mn1;
-  uint32_t pb[kSub][2];
-  float l0 = 0.f, l1 = 0.f;
+    for (int j = 0; j < NS; ++j) {
+      const int tok_a = t0 + j * kChunk + (lane >> 2);
+      const bool va = j < nsub && tok_a < tok_end, vb = j < nsub && tok_a + 8 < tok_end;
+      s[j][nt][0] = va ? s[j][nt][0] * scale_log2 : -INFINITY;
+      s[j][nt][1] = va ? s[j][nt][1] * scale_log2 : -INFINITY;
+      s[j][nt][2] = vb ? s[j][nt][2] * scale_log2 : -INFINITY;
+      s[j][nt][3] = vb ? s[j][nt][3] * scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[j][nt][0], s[j][nt][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[j][nt][1], s[j][nt][3]));
+    }
 #pragma unroll
-  for (int j = 0; j < kSub; ++j) {
-    const float p0 = exp2f(x[j][0] - mn0), p1 = exp2f(x[j][1] - mn1);
-    const float p2 = exp2f(x[j][2] - mn0), p3 = exp2f(x[j][3] - mn1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-    pb[j][0] = movmatrix_trans(Mma<T>::pack(p0, p1));
-    pb[j][1] = movmatrix_trans(Mma<T>::pack(p2, p3));
-  }
-  st.l[0][0] = st.l[0][0] * alpha0 + l0;
-  st.l[0][1] = st.l[0][1] * alpha1 + l1;
-  if (__any_sync(kFullMask, (alpha0 != 1.f) || (alpha1 != 1.f))) {
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m[nt][0], mx0), mn1 = fmaxf(st.m[nt][1], mx1);
+    const float alpha0 = exp2f(st.m[nt][0] - mn0), alpha1 = exp2f(st.m[nt][1] - mn1);
+    st.m[nt][0] = mn0;
+    st.m[nt][1] = mn1;
+    float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      st.o[mt][0][0] *= alpha0;
-      st.o[mt][0][1] *= alpha1;
-      st.o[mt][0][2] *= alpha0;
-      st.o[mt][0][3] *= alpha1;
+    for (int j = 0; j < NS; ++j) {
+      const float p0 = exp2f(s[j][nt][0] - mn0), p1 = exp2f(s[j][nt][1] - mn1);
+      const float p2 = exp2f(s[j][nt][2] - mn0), p3 = exp2f(s[j][nt][3] - mn1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      pb[j][nt][0] = movmatrix_trans(Mma<T>::pack(p0, p1));
+      pb[j][nt][1] = movmatrix_trans(Mma<T>::pack(p2, p3));
+    }
+    st.l[nt][0] = st.l[nt][0] * alpha0 + l0;
+    st.l[nt][1] = st.l[nt][1] * alpha1 + l1;
+    if (__any_sync(kFullMask, (alpha0 != 1.f) || (alpha1 != 1.f))) {
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        st.o[mt][nt][0] *= alpha0;
+        st.o[mt][nt][1] *= alpha1;
+        st.o[mt][nt][2] *= alpha0;
+        st.o[mt][nt][3] *= alpha1;
+      }
     }
   }
   const int v_row = (lane & 7) + ((lane >> 4) << 3);
   const int v_chunk = (lane >> 3) & 1;
 #pragma unroll
-  for (int j = 0; j < kSub; ++j) {
+  for (int j = 0; j < NS; ++j) {
     if (j < nsub) {
       const int tj = t0 + j * kChunk;
       const bool tail = tj + kChunk > tok_end;
@@ -327,75 +340,91 @@ __device__ __forceinline__ void mma_stage4(MmaState<T, D, 1>& st, uint32_t k_bas
           a[2] &= keep_hi;
           a[3] &= keep_hi;
         }
-        Mma<T>::run(st.o[mt][0], a, pb[j]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) Mma<T>::run(st.o[mt][nt], a, pb[j][nt]);
       }
     }
   }
 }
 
-// Query fragments of sequence b's heads h0.. from global memory (group units).
-template <typename T, int D>
-__device__ __forceinline__ void load_q_global(MmaState<T, D, 1>& st, const DecodeParams& p, int b, int h0, int nh,
-                                              int lane) {
+// Query fragments for a prefix-group unit: column tile nt holds heads
+// h0 .. h0+nh-1 of member sequence b0 + nt (zeros past the group's last
+// member), read from global memory; the running state starts empty.
+template <typename T, int D, int NT>
+__device__ __forceinline__ void load_q_members(MmaState<T, D, NT>& st, const DecodeParams& p, int b0,
+                                               int n_members, int h0, int nh, int lane) {
   const int hh = lane >> 2;
-  const bool valid = hh < nh;
-  const T* row = reinterpret_cast<const T*>(p.q) + b * p.q_sb + static_cast<int64_t>(h0 + (valid ? hh : 0)) * p.q_sh;
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    const int d = ks * 16 + 2 * (lane & 3);
-    st.qb[0][ks][0] = valid ? *reinterpret_cast<const uint32_t*>(row + d) : 0u;
-    st.qb[0][ks][1] = valid ? *reinterpret_cast<const uint32_t*>(row + d + 8) : 0u;
+  for (int nt = 0; nt < NT; ++nt) {
+    const bool valid = hh < nh && nt < n_members;
+    const T* row = reinterpret_cast<const T*>(p.q) + (valid ? b0 + nt : 0) * p.q_sb +
+                   static_cast<int64_t>(h0 + (valid ? hh : 0)) * p.q_sh;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int d = ks * 16 + 2 * (lane & 3);
+      st.qb[nt][ks][0] = valid ? *reinterpret_cast<const uint32_t*>(row + d) : 0u;
+      st.qb[nt][ks][1] = valid ? *reinterpret_cast<const uint32_t*>(row + d + 8) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      st.m[nt][j] = -INFINITY;
+      st.l[nt][j] = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.o[mt][nt][e] = 0.f;
   }
-  st.m[0][0] = st.m[0][1] = -INFINITY;
-  st.l[0][0] = st.l[0][1] = 0.f;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) st.o[mt][0][e] = 0.f;
 }
 
-// Finish one sequence of a prefix group (one warp holds all of it): the
-// output when the sequence has one partition, otherwise its partial.
-template <typename T, int D>
-__device__ __forceinline__ void finish_member(MmaState<T, D, 1>& st, const DecodeParams& p, int b, int part,
-                                              int h0, int nh, int lane) {
+// Finish the member sequences b0 .. b0+n_members-1 (column tiles of one warp)
+// of a prefix-group unit over partition `part`: each member's output when it
+// has one partition, otherwise its partial.
+template <typename T, int D, int NT>
+__device__ __forceinline__ void finish_members(MmaState<T, D, NT>& st, const DecodeParams& p, int b0, int n_members,
+                                               int part, int h0, int nh, int lane) {
   const int l_max = p.max_blocks * p.block_size;
-  int L = p.context_lens[b];
-  L = L < 0 ? 0 : (L > l_max ? l_max : L);
-  const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-  float l[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    float v = st.l[0][j];
-    v += __shfl_xor_sync(kFullMask, v, 4);
-    v += __shfl_xor_sync(kFullMask, v, 8);
-    v += __shfl_xor_sync(kFullMask, v, 16);
-    l[j] = v;
-  }
   const int hh = 2 * (lane & 3);
   T* out = reinterpret_cast<T*>(p.out);
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    if (hh + j >= nh) continue;
-    if (n_parts == 1) {
-      const float inv = 1.f / l[j];
-      T* r = out + b * p.o_sb + static_cast<int64_t>(h0 + hh + j) * p.o_sh;
+  for (int nt = 0; nt < NT; ++nt) {
+    if (nt >= n_members) break;
+    const int b = b0 + nt;
+    int L = p.context_lens[b];
+    L = L < 0 ? 0 : (L > l_max ? l_max : L);
+    const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+    float l[2];
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        const int d = mt * 16 + (lane >> 2);
-        r[d] = from_f32<T>(st.o[mt][0][j] * inv);
-        r[d + 8] = from_f32<T>(st.o[mt][0][2 + j] * inv);
-      }
-    } else {
-      const int64_t slot = static_cast<int64_t>(b * p.num_q_heads + h0 + hh + j) * p.max_parts + part;
-      float* wo = p.ws_o + slot * D;
+    for (int j = 0; j < 2; ++j) {
+      float v = st.l[nt][j];
+      v += __shfl_xor_sync(kFullMask, v, 4);
+      v += __shfl_xor_sync(kFullMask, v, 8);
+      v += __shfl_xor_sync(kFullMask, v, 16);
+      l[j] = v;
+    }
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        const int d = mt * 16 + (lane >> 2);
-        wo[d] = st.o[mt][0][j];
-        wo[d + 8] = st.o[mt][0][2 + j];
+    for (int j = 0; j < 2; ++j) {
+      if (hh + j >= nh) continue;
+      if (n_parts == 1) {
+        const float inv = 1.f / l[j];
+        T* r = out + b * p.o_sb + static_cast<int64_t>(h0 + hh + j) * p.o_sh;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d = mt * 16 + (lane >> 2);
+          r[d] = from_f32<T>(st.o[mt][nt][j] * inv);
+          r[d + 8] = from_f32<T>(st.o[mt][nt][2 + j] * inv);
+        }
+      } else {
+        const int64_t slot = static_cast<int64_t>(b * p.num_q_heads + h0 + hh + j) * p.max_parts + part;
+        float* wo = p.ws_o + slot * D;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int d = mt * 16 + (lane >> 2);
+          wo[d] = st.o[mt][nt][j];
+          wo[d + 8] = st.o[mt][nt][2 + j];
+        }
+        if ((lane >> 2) == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(st.m[nt][j], l[j]);
       }
-      if ((lane >> 2) == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(st.m[0][j], l[j]);
     }
   }
 }
@@ -639,11 +668,22 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       return true;
     };
     bool ok = true;
-    int pk = 0;  // pieces handed over
-    auto put_piece = [&](const UnitInfo& x, int c0, int pflags, int e0, int e1) -> bool {
+    int pk = 0;        // pieces handed over
+    int taken = 0;     // pieces the producer is known to have taken
+    int queued = 0;    // work handed over but not yet taken, in stage equivalents
+    int work_reg = 0;  // lane j < Q: work of the last piece put in queue slot j
+    // wait until the producer has taken piece `taken`
+    auto retire = [&]() -> bool {
       bool got = true;
-      if (lane == 0) got = mbar_wait_bounded(smem_u32(qempty + pk % Q), ((pk / Q) & 1) ^ 1, p.wait_limit_ns);
+      if (lane == 0) got = mbar_wait_bounded(smem_u32(qempty + taken % Q), (taken / Q) & 1, p.wait_limit_ns);
       if (__shfl_sync(kFullMask, got ? 1 : 0, 0) == 0) return false;
+      queued -= __shfl_sync(kFullMask, work_reg, taken % Q);
+      ++taken;
+      return true;
+    };
+    auto put_piece = [&](const UnitInfo& x, int c0, int pflags, int e0, int e1, int work) -> bool {
+      while (taken <= pk - Q)  // the slot's previous piece must be taken
+        if (!retire()) return false;
       Piece& pc = pieces[pk % Q];
       if (lane == 0) {
         pc.u = x;
@@ -652,6 +692,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       }
       pc.e[2 * lane] = e0;
       pc.e[2 * lane + 1] = e1;
+      if (lane == pk % Q) work_reg = work;
+      queued += work;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(qfull + pk % Q));
       ++pk;
@@ -660,33 +702,41 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     UnitInfo cur{};
     int e0 = 0, e1 = 0;
     bool have_cur = decode_unit(static_cast<int>(blockIdx.x), cur, e0, e1);
-    int raw_next = 0;  // the next unit id is always requested one unit ahead
-    if (lane == 0 && have_cur) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
     if (flags & kFuseAppend) {
       if (!cta_grid_sync()) ok = false;
     }
     while (ok && have_cur) {
+      // work estimates: a stage, plus one for the unit merge; stages of a
+      // prefix group carry several sequences
+      const int per_stage = cur.group > 1 ? 4 : 1;
       if (cur.group == 0) {
         // covered by its group's leader: nothing to hand over
       } else if (cur.n_chunks == 0) {
-        ok = put_piece(cur, 0, kPieceFirst | kPieceLast, 0, 0);
+        ok = put_piece(cur, 0, kPieceFirst | kPieceLast, 0, 0, 1);
       } else {
         for (int c0 = 0; ok && c0 < cur.n_chunks; c0 += kPieceChunks) {
           if (c0 > 0) load_entries(cur, c0, e0, e1);
-          ok = put_piece(cur, c0, (c0 == 0 ? kPieceFirst : 0) | (c0 + kPieceChunks >= cur.n_chunks ? kPieceLast : 0),
-                         e0, e1);
+          const bool last = c0 + kPieceChunks >= cur.n_chunks;
+          const int stages = (min(kPieceChunks, cur.n_chunks - c0) + kSub - 1) / kSub;
+          ok = put_piece(cur, c0, (c0 == 0 ? kPieceFirst : 0) | (last ? kPieceLast : 0), e0, e1,
+                         stages * per_stage + (last ? 1 : 0));
         }
       }
       if (!ok) break;
-      const int u_nxt = __shfl_sync(kFullMask, raw_next, 0);
+      // claim the next unit only when little work is left queued, so that at
+      // the end no CTA sits on claimed units while others run dry
+      while (ok && taken < pk && queued > kLookahead) ok = retire();
+      if (!ok) break;
+      int u_nxt = 0;
+      if (lane == 0) u_nxt = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
+      u_nxt = __shfl_sync(kFullMask, u_nxt, 0);
       have_cur = decode_unit(u_nxt, cur, e0, e1);
       if (!wait_ok) {
         ok = false;
         break;
       }
-      if (have_cur && lane == 0) raw_next = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);
     }
-    if (!put_piece(UnitInfo{}, 0, kPieceStop, 0, 0)) ok = false;
+    if (!put_piece(UnitInfo{}, 0, kPieceStop, 0, 0, 0)) ok = false;
     if (!ok && lane == 0) atomicOr(p.err, kErrWaitTimeout);
     if (lane == 0) {  // the last CTA to finish leaves the counters at zero for the next launch
       __threadfence();
@@ -865,7 +915,6 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
   }
   if ((flags & kFuseAppend) && !cta_grid_sync()) failed = true;
   MmaState<T, D, NT> st;
-  MmaState<T, D, 1> st2;  // second sequence of a prefix group (group units only)
   const int cw = warp;
   const uint32_t sync_bar = smem_u32(cbar);
   int sync_phase = 0;
@@ -881,22 +930,44 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     if (mt_.flags & kStop) break;
     const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
     if constexpr (kGroupOK) {
-      if (mt_.flags & kGroup) {  // warp cw takes sequences b+cw and b+cw+4 of the group, all 64 tokens
-        const bool has0 = cw < mt_.group, has1 = cw + W < mt_.group;
-        if (mt_.flags & kFirst) {
-          if (has0) load_q_global<T, D>(st, p, mt_.b + cw, mt_.h0, mt_.nh, lane);
-          if (has1) load_q_global<T, D>(st2, p, mt_.b + cw + W, mt_.h0, mt_.nh, lane);
+      if (mt_.flags & kGroup) {
+        // A prefix-group unit, consumed here stage by stage up to its last:
+        // warp cw runs members 2cw and 2cw+1 as the two column tiles of one
+        // state, each stage as two 32-token halves.
+        constexpr int kPerWarp = kMaxGroup / W;
+        static_assert(kPerWarp * W == kMaxGroup, "group members split evenly over the consumers");
+        MmaState<T, D, kPerWarp> gs;
+        const int gb = mt_.b, gpart = mt_.p, gh0 = mt_.h0, gnh = mt_.nh;
+        const int m0 = kPerWarp * cw;
+        const int n_mine = max(0, min(kPerWarp, mt_.group - m0));
+        load_q_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gh0, gnh, lane);
+        int t0 = mt_.t0, tok_end = mt_.tok_end, nsub = mt_.nsub, gflags = mt_.flags;
+        for (;;) {
+          const uint32_t stg = smem_u32(ring + (k % S) * PS::kStageBytes);
+          if (n_mine > 0) {
+            mma_multi<T, D, kPerWarp, 2>(gs, stg, stg + kSub * PS::kKV, t0, tok_end, nsub, p.scale_log2, lane);
+            if (nsub > 2)
+              mma_multi<T, D, kPerWarp, 2>(gs, stg + 2 * PS::kKV, stg + (kSub + 2) * PS::kKV, t0 + 2 * kChunk,
+                                           tok_end, nsub - 2, p.scale_log2, lane);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(empty + k % S));
+          if (gflags & kLast) break;
+          ++k;
+          if (!mbar_wait_bounded(smem_u32(full + k % S), (k / S) & 1, p.wait_limit_ns)) {
+            if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+            failed = true;
+            break;
+          }
+          const StageMeta& gm = meta[k % S];
+          t0 = gm.t0;
+          tok_end = gm.tok_end;
+          nsub = gm.nsub;
+          gflags = gm.flags;
         }
-        if (has0)
-          mma_stage4<T, D>(st, stage, stage + kSub * PS::kKV, mt_.t0, mt_.tok_end, mt_.nsub, p.scale_log2, lane);
-        if (has1)
-          mma_stage4<T, D>(st2, stage, stage + kSub * PS::kKV, mt_.t0, mt_.tok_end, mt_.nsub, p.scale_log2, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(empty + s));
-        if (mt_.flags & kLast) {
-          if (has0) finish_member<T, D>(st, p, mt_.b + cw, mt_.p, mt_.h0, mt_.nh, lane);
-          if (has1) finish_member<T, D>(st2, p, mt_.b + cw + W, mt_.p, mt_.h0, mt_.nh, lane);
-        }
+        if (failed) break;
+        finish_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gpart, gh0, gnh, lane);
+        load_q_members<T, D, NT>(st, p, 0, 0, 0, 0, lane);  // the unit state is not carried past a group unit
         continue;
       }
     }

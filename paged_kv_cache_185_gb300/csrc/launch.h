@@ -68,6 +68,7 @@ int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUten
 int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs);
 constexpr int kPersistentConsumers = 4;
 constexpr int kPersistentMaxSeqs = 1024;      // sequences per launch (the host splits larger batches)
+constexpr int kPersistentMaxParts = 256;      // partitions per sequence (the host widens partitions to fit)
 
 int launch_append(const AppendParams& p, cudaStream_t stream);
 

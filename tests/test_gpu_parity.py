@@ -128,6 +128,23 @@ def test_forced_split_kv(monkeypatch, part, dtype):
     assert torch.equal(got, got2)
 
 
+@pytest.mark.parametrize("B,part", [(300, 256), (1024, 512)])
+def test_split_schedule_with_tied_lengths(monkeypatch, B, part):
+    """Many sequences sharing few distinct lengths (ties in the partition
+    count) split over several partitions: every CTA must derive the same unit
+    order, so each (sequence, partition, kv head) is computed exactly once."""
+    monkeypatch.setenv("WLLM_PARTITION_TOKENS", str(part))
+    rng = torch.Generator().manual_seed(B)
+    lens = [int(x) for x in torch.tensor([part - 3, 2 * part, 2 * part + 5, 3 * part - 1])[
+        torch.randint(0, 4, (B,), generator=rng)]]
+    case = workloads.custom_case("ties", lens=lens, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                                 block_size=16, dtype=torch.float16, seed=B)
+    got, _, _ = gpu_step(case)
+    rows = list(range(0, B * 4, 7)) + [B * 4 - 1]
+    ref, _, _ = oracle_step(case, rows=rows)
+    assert_attention_close(got.reshape(B * 4, -1)[rows], ref, case.dtype, f"ties {B}")
+
+
 def test_fma_variant_matches_oracle(monkeypatch):
     monkeypatch.setenv("WLLM_FORCE_FMA", "1")
     case = workloads.custom_case("fma", lens=LENS, num_q_heads=28, num_kv_heads=4, head_dim=128,

@@ -345,6 +345,8 @@ DecodePlan make_plan(int dt, int64_t B, int64_t hq, int64_t hkv, int64_t d, int6
     pl.grid = static_cast<int>(std::min<int64_t>(n_ctas, std::max<int64_t>(1, B * z * pl.max_parts)));
     pl.separate_combine = pl.max_parts > 1;
     if (pl.max_parts > 1) {
+      // two counters per (sequence, head tile) for the merge inside the launch
+      pl.counter_bytes = align256(size_t(B) * z * 2 * sizeof(int));
       pl.ml_bytes = align256(size_t(B) * hq * pl.max_parts * 2 * sizeof(float));
       pl.o_bytes = align256(size_t(B) * hq * pl.max_parts * d * sizeof(float));
     }
@@ -519,8 +521,10 @@ int wllm_device_errors(void) {
   int word = 0;
   if (cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
   // clearing also resets the persistent kernel's scheduler words, which an
-  // aborted launch may have left non-zero
+  // aborted launch may have left non-zero, and after a timed-out wait (bit 4)
+  // the merge counters
   if (word != 0 && cudaMemset(s->err, 0, 256) != cudaSuccess) return -1;
+  if ((word & 16) && s->counter_bytes > 0 && cudaMemset(s->ws, 0, s->counter_bytes) != cudaSuccess) return -1;
   return word;
 }
 
@@ -657,7 +661,8 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
     if (e != cudaSuccess) return cuda_fail(e, "check_decode launch");
     if ((rc = collect_device_errors(s, st, "paged_attention_decode"))) return rc;
   }
-  // split partitions are merged inside the (cooperative) launch unless asked otherwise
+  // split partitions are merged inside the (cooperative) launch, overlapped
+  // with the decode, unless asked otherwise
   const bool separate_kernel = env_flag("WLLM_SEPARATE_COMBINE");
   const DecodePlan first = make_plan(a.dt, std::min<int64_t>(a.B, kPersistentMaxSeqs), a.hq, a.hkv, a.d, a.mb,
                                      a.bs, a.q_bulk_ok, s->num_sms);
@@ -690,7 +695,7 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = s->err;
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
-    p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 0) != 0;
+    p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 1) != 0;
     if (!pl.persistent && a.hkv * pl.tiles > 65535) return fail(WLLM_ERR_UNSUPPORTED, "too many kv heads");
     if ((rc = bind_workspace(s, pl, st, p))) return rc;
     cudaError_t e;
@@ -910,7 +915,7 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = reinterpret_cast<int*>(scratch);
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
-    p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 0) != 0;
+    p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 1) != 0;
     p.ws_count = nullptr;
     p.ws_ml = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes) : nullptr;
     p.ws_o = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes + pl.ml_bytes) : nullptr;

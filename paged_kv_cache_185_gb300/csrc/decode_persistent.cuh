@@ -46,7 +46,7 @@ constexpr int kGridCountOffset = 48;
 constexpr int kGridGenOffset = 56;
 
 // fused-step flags of one launch
-enum : int { kFuseAppend = 1, kFuseCombine = 2 };
+enum : int { kFuseAppend = 1, kOverlapCombine = 2 };
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -88,6 +88,15 @@ enum : int { kFirst = 1, kLast = 2, kEmptySeq = 4, kStop = 8, kGroup = 16 };
 // kMaxGroup sequences: the K/V bytes are read once for all of them.
 constexpr int kMaxGroup = 8;
 
+// Unit order.  Phase A: partitions below kPhaseAParts, partition-major in
+// sequence order (decoded without a schedule, and a shared prompt prefix --
+// the first partitions -- is handed out early).  Phase B: the later
+// partitions except each sequence's last, sequence-major (prefix sums).
+// Phase C: each sequence's last partition when it lies beyond phase A, in
+// sequence order (ids of sequences without one decode to nothing).  The last
+// partitions are usually partial, so the units handed out last are short.
+constexpr int kPhaseAParts = 2;
+
 constexpr int kSub = 4;                      // 16-token sub-chunks per stage
 constexpr int kStageTokens = kSub * kChunk;  // 64 tokens per stage
 
@@ -113,6 +122,15 @@ struct Piece {
   int e[2 * kPieceChunks];
 };
 static_assert(sizeof(Piece) % 16 == 0, "pieces stay 16-byte aligned");
+
+// A finished unit of split sequences, handed from the consumers to the
+// scheduler warp, which counts it: sequences b .. b+members-1 (a prefix group
+// when members > 1; then only the split ones among them are counted), head
+// tile z.  b < 0: the consumers have stopped.
+struct DoneInfo {
+  int b, z, members, pad;
+};
+constexpr int kDoneSlots = 4;
 
 template <typename T, int D, int NT>
 struct PShape {
@@ -142,14 +160,16 @@ struct PShape {
   static constexpr int kMaxRegs = kMaxRegsRaw > 255 ? 255 : kMaxRegsRaw;
   static constexpr int kSeqBytes = ((kPersistentMaxSeqs + 1) * 4 + 15) / 16 * 16;
   static constexpr int kSmemPerCta = 233472 / kCtasPerSm - 1024;
-  static constexpr int kQueueBytes = kQueue * (static_cast<int>(sizeof(Piece)) + 16);
+  static constexpr int kQueueBytes =
+      kQueue * (static_cast<int>(sizeof(Piece)) + 16) + kDoneSlots * (static_cast<int>(sizeof(DoneInfo)) + 16) + 16;
   static constexpr int kStagesRaw = (kSmemPerCta - 1024 - 64 - 16 - kSeqBytes - kQueueBytes) / (kStageBytes + 64);
   static constexpr int kStages = kStagesRaw > 16 ? 16 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kBarBytes = (2 * kStages + 2 + 2 * kQueue) * 8;
+  static constexpr int kBarBytes = (2 * kStages + 2 + 2 * kQueue + 2 * kDoneSlots) * 8;
   static constexpr int kMetaBytes = kStages * static_cast<int>(sizeof(StageMeta));
+  static constexpr int kDoneBytes = kDoneSlots * static_cast<int>(sizeof(DoneInfo));
   static constexpr int kFixedSmem =
-      1024 + kRingBytes + kBarBytes + kMetaBytes + kQueue * static_cast<int>(sizeof(Piece)) + 64;
+      1024 + kRingBytes + kBarBytes + kMetaBytes + kQueue * static_cast<int>(sizeof(Piece)) + kDoneBytes + 64;
 };
 
 // Query fragments of a unit from the stage's query rows (row stride D).
@@ -188,59 +208,103 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, int& phase, uint64_t
   return __all_sync(kFullMask, ok);
 }
 
-// Merge the partitions of one query row (b, h): weights exp2(m_p - M), fp32
-// sums, round-to-nearest into `out`.  One warp; rows with one partition were
-// written by the decode itself.
-template <typename T, int D>
-__device__ __forceinline__ void combine_row(const DecodeParams& p, int row, int lane) {
-  const int b = row / p.num_q_heads;
-  int L = p.context_lens[b];
+// Merge the partitions of R query rows at once (one warp): for each row
+// (b, h), weights exp2(m_p - M) with M the largest m_p, fp32 sums,
+// round-to-nearest into `out`.  Lane l owns dims [l*D/32, (l+1)*D/32), so a
+// partial is one or two vector loads per lane.  Two memory round trips cover
+// all R rows when each has at most kBatch partitions: the context lengths,
+// then every (m, l) pair and partial at once.  rows[r] < 0 skips slot r; rows
+// with one partition were written by the decode itself.
+template <typename T, int D, int R>
+__device__ __forceinline__ void combine_rows(const DecodeParams& p, const int (&rows)[R], int lane) {
+  constexpr int V = D / 32;
+  constexpr int kBatch = 32 / V;
   const int l_max = p.max_blocks * p.block_size;
-  L = L < 0 ? 0 : (L > l_max ? l_max : L);
-  const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-  if (n_parts == 1) return;
-  const int64_t base = static_cast<int64_t>(row) * p.max_parts;
-  const float2* ml = reinterpret_cast<const float2*>(p.ws_ml);
-  float M = -INFINITY;
-  for (int pp = lane; pp < n_parts; pp += 32) M = fmaxf(M, __ldcg(ml + base + pp).x);
+  int n[R];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
-  float den = 0.f, num[D / 32];
+  for (int r = 0; r < R; ++r) {
+    int L = rows[r] >= 0 ? p.context_lens[rows[r] / p.num_q_heads] : 0;
+    L = L < 0 ? 0 : (L > l_max ? l_max : L);
+    n[r] = (rows[r] < 0 || L == 0) ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  }
+  auto load_part = [&](const float* src, float* dst) {
+    if constexpr (V >= 4) {
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) num[i] = 0.f;
-  for (int p0 = 0; p0 < n_parts; p0 += 32) {
-    const bool mine = p0 + lane < n_parts;
-    const float2 v = mine ? __ldcg(ml + base + p0 + lane) : make_float2(-INFINITY, 0.f);
-    const float f = mine ? exp2f(v.x - M) : 0.f;
-    den += f * v.y;
-    const int cnt = min(32, n_parts - p0);
-    // eight partitions per batch, every load issued before the first use
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float o[8][D / 32];
+      for (int i = 0; i < V; i += 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + i));
+        dst[i] = x.x;
+        dst[i + 1] = x.y;
+        dst[i + 2] = x.z;
+        dst[i + 3] = x.w;
+      }
+    } else {
+      const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+      dst[0] = x.x;
+      dst[1] = x.y;
+    }
+  };
+  float2 v[R];
+  float o[R][kBatch][V];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j0 + j < cnt) {
-          const float* src = p.ws_o + (base + p0 + j0 + j) * D;
+  for (int r = 0; r < R; ++r) {
+    if (n[r] < 2) continue;
+    const int64_t base = static_cast<int64_t>(rows[r]) * p.max_parts;
+    v[r] = lane < min(32, n[r]) ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base + lane)
+                                : make_float2(-INFINITY, 0.f);
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) o[j][i] = __ldcg(src + lane + 32 * i);
+    for (int j = 0; j < kBatch; ++j)
+      if (j < n[r]) load_part(p.ws_o + (base + j) * D + lane * V, o[r][j]);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (n[r] < 2) continue;
+    const int64_t base = static_cast<int64_t>(rows[r]) * p.max_parts;
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    float M = -INFINITY, den = 0.f;
+    for (int p0 = 0; p0 < n[r]; p0 += 32) {  // groups of 32 partitions, one (m, l) per lane
+      const int cnt = min(32, n[r] - p0);
+      float2 w = v[r];
+      if (p0 > 0) w = lane < cnt ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base + p0 + lane)
+                                 : make_float2(-INFINITY, 0.f);
+      float mg = w.x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mg = fmaxf(mg, __shfl_xor_sync(kFullMask, mg, off));
+      const float Mn = fmaxf(M, mg);
+      const float rescale = exp2f(M - Mn);  // 0 for the first group
+      M = Mn;
+      den *= rescale;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] *= rescale;
+      const float f = lane < cnt ? exp2f(w.x - M) : 0.f;
+      float dsum = f * w.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(kFullMask, dsum, off);
+      den += dsum;
+      for (int j0 = 0; j0 < cnt; j0 += kBatch) {
+        if (p0 + j0 > 0) {
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            if (j0 + j < cnt) load_part(p.ws_o + (base + p0 + j0 + j) * D + lane * V, o[r][j]);
         }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float fp = __shfl_sync(kFullMask, f, (j0 + j) & 31);
-        if (j0 + j < cnt) {
+        for (int j = 0; j < kBatch; ++j) {
+          const float fp = __shfl_sync(kFullMask, f, (j0 + j) & 31);
+          if (j0 + j < cnt) {
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) num[i] = fmaf(fp, o[j][i], num[i]);
+            for (int i = 0; i < V; ++i) acc[i] = fmaf(fp, o[r][j][i], acc[i]);
+          }
         }
       }
     }
+    const float inv = 1.f / den;
+    const int b = rows[r] / p.num_q_heads;
+    const int h = rows[r] - b * p.num_q_heads;
+    T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh + lane * V;
+#pragma unroll
+    for (int i = 0; i < V; ++i) orow[i] = from_f32<T>(acc[i] * inv);
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(kFullMask, den, off);
-  const float inv = 1.f / den;
-  const int h = row - b * p.num_q_heads;
-  T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh;
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(num[i] * inv);
 }
 
 // NS consecutive 16-token sub-chunks (sub-chunk j's K at k_base + j * kKV,
@@ -450,9 +514,12 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
   uint64_t* pbar = cbar + 1;                  // prefix sums ready (consumers -> scheduler)
   uint64_t* qfull = pbar + 1;                 // piece queue: scheduler -> producer
   uint64_t* qempty = qfull + kQueue;
-  StageMeta* meta = reinterpret_cast<StageMeta*>(qempty + kQueue);
+  uint64_t* done_full = qempty + kQueue;      // finished split units: consumers -> scheduler
+  uint64_t* done_empty = done_full + kDoneSlots;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(done_empty + kDoneSlots);
   Piece* pieces = reinterpret_cast<Piece*>(meta + S);
-  int* wsum = reinterpret_cast<int*>(pieces + kQueue);  // 16 ints of scratch
+  DoneInfo* done_info = reinterpret_cast<DoneInfo*>(pieces + kQueue);
+  int* wsum = reinterpret_cast<int*>(done_info + kDoneSlots);  // 16 ints of scratch
   int* prefix = wsum + 16;                       // [B + 1] units before sequence b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -470,6 +537,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     for (int i = 0; i < Q; ++i) {
       mbar_init(smem_u32(qfull + i), 1);
       mbar_init(smem_u32(qempty + i), 1);
+    }
+    for (int i = 0; i < kDoneSlots; ++i) {
+      mbar_init(smem_u32(done_full + i), W);
+      mbar_init(smem_u32(done_empty + i), 1);
     }
     fence_mbar_init();
   }
@@ -527,16 +598,17 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       }
     };
     // Sharing of the full partition starting at token tb of sequence b with its
-    // neighbours: returns 0 when an earlier sequence's group covers b, else
-    // the number of sequences b.. (at most kMaxGroup) whose tables name the
-    // same physical blocks for the whole partition.  Block lists are compared
-    // a warp at a time (up to 64 blocks: two per lane); rows are loaded in
-    // batches (b-1..b+1 first, the rest only when a neighbour shares) so the
-    // check costs one or two round trips.
+    // neighbours.  Groups are the runs of consecutive sequences whose tables
+    // name the same physical blocks for the whole partition, cut at every
+    // multiple of kMaxGroup: sequence b leads a group unless b - 1 shares with
+    // it and b is not a multiple of kMaxGroup.  Returns 0 for a covered
+    // sequence, else the group's size (1: no sharing).  Block lists are
+    // compared a warp at a time (up to 64 blocks: two per lane); the rows
+    // needed (b - 1 .. the group's end) are loaded in one batch.
     auto prefix_group = [&](int b, int tb) -> int {
       const int nblk = p.part_tokens >> p.log2_bs;
       const int j0 = tb >> p.log2_bs;
-      constexpr int R = kMaxGroup - 1;  // rows each side
+      const int span = kMaxGroup - (b % kMaxGroup);  // b .. b+span-1 may form b's group
       auto load_row = [&](int bb, int& v0, int& v1) {
         v0 = -1;
         v1 = -1;
@@ -546,55 +618,31 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
           if (lane + 32 < nblk) v1 = r[lane + 32];
         }
       };
-      // lane i < 2R+1 holds whether row b-R+i fills the partition
-      auto covers_mask = [&]() -> unsigned {
-        const int bb = b - R + lane;
-        bool c = false;
-        if (lane < 2 * R + 1 && bb >= 0 && bb < B) {
-          int Lb = p.context_lens[bb];
-          Lb = Lb < 0 ? 0 : (Lb > l_max ? l_max : Lb);
-          c = Lb >= tb + p.part_tokens;
-        }
-        return __ballot_sync(kFullMask, c);
-      };
-      int c0, c1, a0, a1, n0, n1;
-      load_row(b, c0, c1);
-      load_row(b - 1, a0, a1);
-      load_row(b + 1, n0, n1);
-      const unsigned cov = covers_mask();
-      const bool prev = b > 0 && ((cov >> (R - 1)) & 1) && __all_sync(kFullMask, a0 == c0 && a1 == c1);
-      const bool next = b + 1 < B && ((cov >> (R + 1)) & 1) && __all_sync(kFullMask, n0 == c0 && n1 == c1);
-      if (!prev && !next) return 1;
-      int r0[2 * R + 1], r1[2 * R + 1];
-#pragma unroll
-      for (int i = 0; i < 2 * R + 1; ++i) load_row(b - R + i, r0[i], r1[i]);
-      unsigned same = 0;  // bit i: row b-R+i names the same blocks and fills the partition
-#pragma unroll
-      for (int i = 0; i < 2 * R + 1; ++i)
-        if (__all_sync(kFullMask, r0[i] == c0 && r1[i] == c1) && ((cov >> i) & 1)) same |= 1u << i;
-      int k = 0;  // sharing predecessors in a row
-      while (k < R && ((same >> (R - 1 - k)) & 1)) ++k;
-      if (k > 0) {
-        // the run's first sequence leads a group of up to kMaxGroup; so does
-        // every kMaxGroup-th one after it (a run longer than R back is
-        // rechecked from further back only in that rare case)
-        int run = k;
-        if (k == R) {
-          int bb = b - R - 1;
-          while (bb >= 0 && run % kMaxGroup != 0) {
-            int x0, x1;
-            load_row(bb, x0, x1);
-            int Lb = p.context_lens[bb];
-            Lb = Lb < 0 ? 0 : (Lb > l_max ? l_max : Lb);
-            if (!(__all_sync(kFullMask, x0 == c0 && x1 == c1) && Lb >= tb + p.part_tokens)) break;
-            ++run;
-            --bb;
-          }
-        }
-        if (run % kMaxGroup != 0) return 0;
+      // lane i <= kMaxGroup: whether row b-1+i fills the partition
+      const int bb_l = b - 1 + lane;
+      bool cov = false;
+      if (lane <= kMaxGroup && bb_l >= 0 && bb_l < B) {
+        int Lb = p.context_lens[bb_l];
+        Lb = Lb < 0 ? 0 : (Lb > l_max ? l_max : Lb);
+        cov = Lb >= tb + p.part_tokens;
       }
+      const unsigned covm = __ballot_sync(kFullMask, cov);
+      int r0[kMaxGroup + 1], r1[kMaxGroup + 1];  // rows b-1 .. b+kMaxGroup-1
+#pragma unroll
+      for (int i = 0; i <= kMaxGroup; ++i) {
+        if (i == 0 || i <= span) load_row(b - 1 + i, r0[i], r1[i]);
+        else r0[i] = r1[i] = -1;
+      }
+      const int c0 = r0[1], c1 = r1[1];  // sequence b's own blocks
+      auto same = [&](int i) {  // row b-1+i names b's blocks and fills the partition
+        return ((covm >> i) & 1) && __all_sync(kFullMask, r0[i] == c0 && r1[i] == c1);
+      };
+      if (b % kMaxGroup != 0 && b > 0 && same(0)) return 0;
       int g = 1;
-      while (g < kMaxGroup && ((same >> (R + g)) & 1)) ++g;
+#pragma unroll
+      for (int i = 2; i <= kMaxGroup; ++i) {
+        if (g == i - 1 && i <= span && same(i)) g = i;
+      }
       return g;
     };
     bool have_prefix = false;
@@ -604,24 +652,30 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     // false past the last unit.
     auto decode_unit = [&](int u, UnitInfo& x, int& e0, int& e1) -> bool {
       int L;
-      if (u < BZ) {
-        x.b = u / Z;
-        x.z = u - x.b * Z;
-        x.part = 0;
+      if (u < kPhaseAParts * BZ) {
+        x.part = u / BZ;
+        const int r = u - x.part * BZ;
+        x.b = r / Z;
+        x.z = r - x.b * Z;
         int Lraw = p.context_lens[x.b];  // issued together with the table loads below
         const int32_t* bt_row = p.block_tables + static_cast<int64_t>(x.b) * p.bt_stride;
-        const int j0 = (kChunk * lane) >> p.log2_bs;
+        x.tb = x.part * p.part_tokens;
+        const int j0 = (x.tb + kChunk * lane) >> p.log2_bs;
         int r0 = j0 < p.max_blocks ? bt_row[j0] : 0;
         int r1 = (p.log2_bs < 4 && j0 + 1 < p.max_blocks) ? bt_row[j0 + 1] : 0;
         if (Lraw < 0 || Lraw > l_max) {
-          if (lane == 0) atomicOr(p.err, kErrLen);
+          if (lane == 0 && x.part == 0) atomicOr(p.err, kErrLen);
           Lraw = Lraw < 0 ? 0 : l_max;
         }
         L = Lraw;
-        x.tb = 0;
-        x.te = min(L, p.part_tokens);
-        x.n_chunks = L == 0 ? 0 : (x.te + kChunk - 1) / kChunk;
-        const int t0 = kChunk * lane;
+        if (x.part > 0 && L <= x.tb) {  // the sequence has no such partition: nothing to do
+          x.group = 0;
+          x.n_chunks = 0;
+          return true;
+        }
+        x.te = min(L, x.tb + p.part_tokens);
+        x.n_chunks = L == 0 ? 0 : (x.te - x.tb + kChunk - 1) / kChunk;
+        const int t0 = x.tb + kChunk * lane;
         const bool need0 = lane < x.n_chunks, need1 = need0 && p.log2_bs < 4 && t0 + 8 < x.te;
         if ((need0 && (r0 < 0 || r0 >= p.num_blocks)) || (need1 && (r1 < 0 || r1 >= p.num_blocks))) {
           atomicOr(p.err, kErrBlock);
@@ -636,24 +690,43 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
           have_prefix = true;
           if (!wait_ok) return false;
         }
-        const int u2 = u - BZ;
-        if (u2 >= prefix[B]) return false;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (prefix[mid] <= u2) lo = mid;
-          else hi = mid - 1;
+        const int u2 = u - kPhaseAParts * BZ;
+        if (u2 >= prefix[B]) {  // phase C
+          const int u3 = u2 - prefix[B];
+          if (u3 >= BZ) return false;
+          x.b = u3 / Z;
+          x.z = u3 - x.b * Z;
+          L = p.context_lens[x.b];
+          L = L < 0 ? 0 : (L > l_max ? l_max : L);
+          const int np = (L + p.part_tokens - 1) / p.part_tokens;
+          if (np <= kPhaseAParts) {  // its last partition was in phase A
+            x.group = 0;
+            x.n_chunks = 0;
+            return true;
+          }
+          x.part = np - 1;
+          x.tb = x.part * p.part_tokens;
+          x.te = L;
+          x.n_chunks = (x.te - x.tb + kChunk - 1) / kChunk;
+          load_entries(x, 0, e0, e1);
+        } else {
+          int lo = 0, hi = B - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= u2) lo = mid;
+            else hi = mid - 1;
+          }
+          x.b = lo;
+          const int r = u2 - prefix[lo];
+          x.part = kPhaseAParts + r / Z;
+          x.z = r - (r / Z) * Z;
+          L = p.context_lens[lo];  // checked and clamped by the consumers' prefix pass
+          L = L < 0 ? 0 : (L > l_max ? l_max : L);
+          x.tb = x.part * p.part_tokens;
+          x.te = min(L, x.tb + p.part_tokens);
+          x.n_chunks = (x.te - x.tb + kChunk - 1) / kChunk;
+          load_entries(x, 0, e0, e1);
         }
-        x.b = lo;
-        const int r = u2 - prefix[lo];
-        x.part = 1 + r / Z;
-        x.z = r - (r / Z) * Z;
-        L = p.context_lens[lo];  // checked and clamped by the consumers' prefix pass
-        L = L < 0 ? 0 : (L > l_max ? l_max : L);
-        x.tb = x.part * p.part_tokens;
-        x.te = min(L, x.tb + p.part_tokens);
-        x.n_chunks = (x.te - x.tb + kChunk - 1) / kChunk;
-        load_entries(x, 0, e0, e1);
       }
       x.n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
       x.kvh = x.z / p.num_head_tiles;
@@ -667,6 +740,53 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       }
       return true;
     };
+    // Finished units of split sequences (the consumers' done ring): each is
+    // counted on its (sequence, head tile) counter, which the merge at the
+    // end of the launch waits on.  The fence publishes the partials the
+    // consumers wrote before arriving on the ring.  Never blocks.
+    int dd = 0;  // ring records taken
+    bool consumers_done = (flags & kOverlapCombine) == 0;
+    auto service = [&]() {
+      while (!consumers_done) {
+        const int slot = dd % kDoneSlots;
+        bool ready = false;
+        if (lane == 0) ready = mbar_test_wait(smem_u32(done_full + slot), (dd / kDoneSlots) & 1);
+        if (__shfl_sync(kFullMask, ready ? 1 : 0, 0) == 0) return;
+        const DoneInfo di = done_info[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(done_empty + slot));
+        ++dd;
+        if (di.b < 0) {
+          consumers_done = true;
+          return;
+        }
+        __threadfence();
+        if (lane < di.members) {
+          const int bm = di.b + lane;
+          bool split = true;
+          if (di.members > 1) {  // group members: only split sequences are merged
+            int L = p.context_lens[bm];
+            L = L < 0 ? 0 : (L > l_max ? l_max : L);
+            split = L > p.part_tokens;
+          }
+          if (split) atomicAdd(p.ws_count + static_cast<int64_t>(bm) * Z + di.z, 1);
+        }
+      }
+    };
+    // poll `bar` for phase `parity`, serving the done ring meanwhile (bounded)
+    auto wait_serving = [&](uint64_t* bar, int parity) -> bool {
+      uint64_t t0 = 0;
+      if (lane == 0) t0 = global_timer_ns();
+      while (true) {
+        bool got = false;
+        if (lane == 0) got = mbar_test_wait(smem_u32(bar), parity);
+        if (__shfl_sync(kFullMask, got ? 1 : 0, 0) != 0) return true;
+        service();
+        bool late = false;
+        if (lane == 0) late = global_timer_ns() - t0 > p.wait_limit_ns;
+        if (__shfl_sync(kFullMask, late ? 1 : 0, 0) != 0) return false;
+      }
+    };
     bool ok = true;
     int pk = 0;        // pieces handed over
     int taken = 0;     // pieces the producer is known to have taken
@@ -674,9 +794,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     int work_reg = 0;  // lane j < Q: work of the last piece put in queue slot j
     // wait until the producer has taken piece `taken`
     auto retire = [&]() -> bool {
-      bool got = true;
-      if (lane == 0) got = mbar_wait_bounded(smem_u32(qempty + taken % Q), (taken / Q) & 1, p.wait_limit_ns);
-      if (__shfl_sync(kFullMask, got ? 1 : 0, 0) == 0) return false;
+      if (!wait_serving(qempty + taken % Q, (taken / Q) & 1)) return false;
       queued -= __shfl_sync(kFullMask, work_reg, taken % Q);
       ++taken;
       return true;
@@ -723,6 +841,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
         }
       }
       if (!ok) break;
+      service();
       // claim the next unit only when little work is left queued, so that at
       // the end no CTA sits on claimed units while others run dry
       while (ok && taken < pk && queued > kLookahead) ok = retire();
@@ -737,6 +856,19 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       }
     }
     if (!put_piece(UnitInfo{}, 0, kPieceStop, 0, 0, 0)) ok = false;
+    if (ok && !consumers_done) {  // serve the consumers until their last unit is counted
+      uint64_t t0 = 0;
+      if (lane == 0) t0 = global_timer_ns();
+      while (!consumers_done) {
+        service();
+        bool late = false;
+        if (lane == 0) late = global_timer_ns() - t0 > p.wait_limit_ns;
+        if (__shfl_sync(kFullMask, late ? 1 : 0, 0) != 0) {
+          ok = false;
+          break;
+        }
+      }
+    }
     if (!ok && lane == 0) atomicOr(p.err, kErrWaitTimeout);
     if (lane == 0) {  // the last CTA to finish leaves the counters at zero for the next launch
       __threadfence();
@@ -881,8 +1013,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
   } else {
 
   // ------------------------------- consumers --------------------------------
-  // prefix sums of the units at partitions >= 1, sequence-major, and the
-  // clamped lengths; then tell the producer
+  // prefix sums of the phase-B units (partitions >= kPhaseAParts but the
+  // last), sequence-major; then tell the scheduler
   {
     constexpr int kCT = W * 32;
     const int per = (B + kCT - 1) / kCT;
@@ -891,7 +1023,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     for (int b = lo; b < hi; ++b) {
       int L = p.context_lens[b];
       L = L < 0 ? 0 : (L > l_max ? l_max : L);
-      local += (L == 0 ? 0 : (L + p.part_tokens - 1) / p.part_tokens - 1) * Z;
+      local += max(0, (L + p.part_tokens - 1) / p.part_tokens - kPhaseAParts - 1) * Z;
     }
     int incl = local;
 #pragma unroll
@@ -907,7 +1039,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       prefix[b] = run;
       int L = p.context_lens[b];
       L = L < 0 ? 0 : (L > l_max ? l_max : L);
-      run += (L == 0 ? 0 : (L + p.part_tokens - 1) / p.part_tokens - 1) * Z;
+      run += max(0, (L + p.part_tokens - 1) / p.part_tokens - kPhaseAParts - 1) * Z;
     }
     if (threadIdx.x == kCT - 1) prefix[B] = wsum[0] + wsum[1] + wsum[2] + wsum[3];
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
@@ -918,6 +1050,24 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
   const int cw = warp;
   const uint32_t sync_bar = smem_u32(cbar);
   int sync_phase = 0;
+  int dk = 0;  // records handed to the scheduler
+  // Every consumer warp arrives on the record's barrier after writing its
+  // partials; warp 0 first takes the slot (freed by the scheduler) and fills it.
+  auto post_done = [&](const DoneInfo& di) -> bool {
+    const int slot = dk % kDoneSlots;
+    bool ok = true;
+    if (cw == 0) {
+      if (lane == 0) ok = mbar_wait_bounded(smem_u32(done_empty + slot), ((dk / kDoneSlots) & 1) ^ 1, p.wait_limit_ns);
+      ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+      if (ok && lane == 0) done_info[slot] = di;
+    }
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(smem_u32(done_full + slot));
+    ++dk;
+    if (!ok && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+    return ok;
+  };
+  const bool count_units = (flags & kOverlapCombine) != 0;
   T* out = reinterpret_cast<T*>(p.out);
   for (int k = 0; !failed; ++k) {
     const int s = k % S;
@@ -937,7 +1087,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
         constexpr int kPerWarp = kMaxGroup / W;
         static_assert(kPerWarp * W == kMaxGroup, "group members split evenly over the consumers");
         MmaState<T, D, kPerWarp> gs;
-        const int gb = mt_.b, gpart = mt_.p, gh0 = mt_.h0, gnh = mt_.nh;
+        const int gb = mt_.b, gpart = mt_.p, gh0 = mt_.h0, gnh = mt_.nh, gz = mt_.z;
         const int m0 = kPerWarp * cw;
         const int n_mine = max(0, min(kPerWarp, mt_.group - m0));
         load_q_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gh0, gnh, lane);
@@ -967,6 +1117,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
         }
         if (failed) break;
         finish_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gpart, gh0, gnh, lane);
+        if (count_units && !post_done(DoneInfo{gb, gz, mt_.group, 0})) {
+          failed = true;
+          break;
+        }
         load_q_members<T, D, NT>(st, p, 0, 0, 0, 0, lane);  // the unit state is not carried past a group unit
         continue;
       }
@@ -1053,17 +1207,76 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    if (split && count_units && !post_done(DoneInfo{b, mt_.z, 1, 0})) {
+      failed = true;
+      break;
+    }
   }
+  if (count_units && !failed && !post_done(DoneInfo{-1, 0, 0, 0})) failed = true;  // no more units
   }  // consumers
 
   // fused step: once every CTA's partials are written, all warps of all CTAs
   // merge the split rows (one warp per query row)
-  if (flags & kFuseCombine) {
-    if (cta_grid_sync() && !failed) {
-      const int gwarp = static_cast<int>(blockIdx.x) * (W + 2) + warp;
-      for (int row = gwarp; row < B * p.num_q_heads; row += static_cast<int>(gridDim.x) * (W + 2))
-        combine_row<T, D>(p, row, lane);
+  // Merge of split sequences, overlapped with other CTAs' decode: warp g of
+  // the launch takes rows g, g + (warps in the launch), ...; each row waits
+  // (bounded) until every unit of its (sequence, head tile) has been counted,
+  // then merges.  The last row of a (sequence, head tile) puts its two
+  // counters back to zero.  Every CTA is resident (cooperative launch), so
+  // the waits end.
+  if ((flags & kOverlapCombine) && !failed) {
+    const int nw = static_cast<int>(gridDim.x) * (W + 2);
+    const int gwarp = static_cast<int>(blockIdx.x) * (W + 2) + warp;
+    const int n_rows = B * p.num_q_heads;
+    int* count = p.ws_count;
+    int* rows_done = p.ws_count + B * Z;
+    int pend_old = 0, pend_bz = -1, pend_nh = 0;  // row-count arrival whose result is read one row later
+    auto settle = [&]() {
+      if (pend_bz < 0) return;
+      const int old = __shfl_sync(kFullMask, pend_old, 0);
+      if (old == pend_nh - 1 && lane == 0) {
+        count[pend_bz] = 0;
+        rows_done[pend_bz] = 0;
+      }
+      pend_bz = -1;
+    };
+    for (int row = gwarp; row < n_rows; row += nw) {
+      const int b = row / p.num_q_heads;
+      const int h = row - b * p.num_q_heads;
+      int L = p.context_lens[b];
+      L = L < 0 ? 0 : (L > l_max ? l_max : L);
+      const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+      if (n_parts < 2) continue;
+      const int kvh = h / p.group;
+      const int tile = (h - kvh * p.group) / HT;
+      const int bz = b * Z + kvh * p.num_head_tiles + tile;
+      const int nh_z = min(HT, p.group - tile * HT);
+      bool ready = true;
+      if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+          int c;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(c) : "l"(count + bz) : "memory");
+          if (c >= n_parts) break;
+          if (global_timer_ns() - t0 > p.wait_limit_ns) {
+            ready = false;
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+      if (__shfl_sync(kFullMask, ready ? 1 : 0, 0) == 0) {
+        if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+        break;
+      }
+      __syncwarp();  // lane 0's acquire orders every lane's partial loads below
+      const int rows1[1] = {row};
+      combine_rows<T, D, 1>(p, rows1, lane);
+      settle();
+      if (lane == 0) pend_old = atomicAdd(rows_done + bz, 1);
+      pend_bz = bz;
+      pend_nh = nh_z;
     }
+    settle();
   }
 }
 
@@ -1073,7 +1286,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= p.num_seqs * p.num_q_heads) return;
-  combine_row<T, D>(p, row, threadIdx.x & 31);
+  const int rows[1] = {row};
+  combine_rows<T, D, 1>(p, rows, threadIdx.x & 31);
 }
 
 template <typename T, int D, int NT>
@@ -1082,10 +1296,12 @@ int persistent_smem(int num_seqs) {
 }
 
 // Launch the persistent decode.  `ap` non-null fuses the KV append in front of
-// the decode; `fuse_combine` merges split partitions inside the launch.  Either
-// makes the launch cooperative (grid barriers need every CTA resident; the grid
-// never exceeds SMs x occupancy).  Otherwise split partitions are merged by
-// the separate combine kernel when `separate_combine` is set.
+// the decode (behind a grid barrier); `fuse_combine` merges split partitions
+// inside the launch (p.ws_count: two zeroed counters per sequence and head
+// tile).  Either makes the launch cooperative (the barrier and the merge's
+// waits need every CTA resident; the grid never exceeds SMs x occupancy).
+// Otherwise split partitions are merged by the separate combine kernel when
+// `separate_combine` is set.
 template <typename T, int D, int NT>
 int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p, int grid,
                            bool separate_combine, const AppendParams* ap, bool fuse_combine,
@@ -1104,7 +1320,7 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
   }
   AppendParams none{};
   const AppendParams& app = ap != nullptr ? *ap : none;
-  const int flags = (ap != nullptr ? kFuseAppend : 0) | (fuse_combine ? kFuseCombine : 0);
+  const int flags = (ap != nullptr ? kFuseAppend : 0) | (fuse_combine ? kOverlapCombine : 0);
   if (flags == 0) {
     kernel<<<grid, PS::kThreads, smem, stream>>>(kmap, vmap, p, app, flags);
   } else {

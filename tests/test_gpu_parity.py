@@ -450,16 +450,34 @@ def test_fused_step_shapes(dtype, Hq, Hkv, D, bs):
     assert_attention_close(got, ref, dtype, f"fused {dtype} {Hq}/{Hkv} D{D} bs{bs}")
 
 
-def test_separate_combine_kernel(monkeypatch):
-    monkeypatch.setenv("WLLM_SEPARATE_COMBINE", "1")
+@pytest.mark.parametrize("D,Hq,Hkv,dtype", [(64, 32, 4, torch.float16), (256, 8, 1, torch.bfloat16),
+                                           (128, 32, 32, torch.bfloat16)])
+def test_split_merge_head_dims(monkeypatch, D, Hq, Hkv, dtype):
+    """In-launch merge of split sequences at every head_dim, twice in a row
+    (scheduler and barrier words must be back at zero after each launch)."""
+    monkeypatch.setenv("WLLM_PARTITION_TOKENS", "128")
+    lens = [1, 129, 700, 2049, 0, 1300, 128, 257]
+    case = workloads.custom_case("merge", lens=lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                                 block_size=16, dtype=dtype, seed=D + Hq, heavy_key_frac=0.02)
+    got, _, _ = gpu_step(case)
+    ref, _, _ = oracle_step(case)
+    assert_attention_close(got, ref, dtype, f"merge D{D}")
+    got2, _, _ = fused_step(case)
+    assert torch.equal(int_view(got), int_view(got2))
+
+
+@pytest.mark.parametrize("mode", ["WLLM_SEPARATE_COMBINE"])
+def test_other_combine_modes(monkeypatch, mode):
+    """Split partitions merged by a second kernel instead of inside the launch."""
+    monkeypatch.setenv(mode, "1")
     monkeypatch.setenv("WLLM_PARTITION_TOKENS", "128")
     case = workloads.custom_case("sep", lens=[5, 900, 2500, 1], num_q_heads=8, num_kv_heads=2,
                                  head_dim=64, block_size=16, dtype=torch.float16, seed=44)
     got, _, _ = gpu_step(case)
     ref, _, _ = oracle_step(case)
-    assert_attention_close(got, ref, case.dtype, "separate combine")
+    assert_attention_close(got, ref, case.dtype, mode)
     got2, _, _ = fused_step(case)
-    assert_attention_close(got2, ref, case.dtype, "separate combine, step")
+    assert_attention_close(got2, ref, case.dtype, mode + ", step")
 
 
 def test_fused_step_without_tokens_or_sequences():

@@ -113,7 +113,7 @@ struct UnitInfo {
 constexpr int kPieceChunks = 32;
 constexpr int kQueue = 4;  // pieces in flight between scheduler and producer
 // The scheduler claims another unit only when at most this much work (in
-// 64-token stage equivalents) waits in the queue.
+// 64-token stage equivalents) waits in its queue.
 constexpr int kLookahead = 8;
 enum : int { kPieceFirst = 1, kPieceLast = 2, kPieceStop = 4 };
 struct Piece {
@@ -748,28 +748,37 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     bool consumers_done = (flags & kOverlapCombine) == 0;
     auto service = [&]() {
       while (!consumers_done) {
-        const int slot = dd % kDoneSlots;
-        bool ready = false;
-        if (lane == 0) ready = mbar_test_wait(smem_u32(done_full + slot), (dd / kDoneSlots) & 1);
-        if (__shfl_sync(kFullMask, ready ? 1 : 0, 0) == 0) return;
-        const DoneInfo di = done_info[slot];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(done_empty + slot));
-        ++dd;
-        if (di.b < 0) {
-          consumers_done = true;
-          return;
+        // take every record that is ready, then one fence for all of them
+        DoneInfo rec[kDoneSlots];
+        int nrec = 0;
+#pragma unroll
+        for (int i = 0; i < kDoneSlots; ++i) {
+          if (nrec != i || consumers_done) break;
+          const int slot = dd % kDoneSlots;
+          bool ready = false;
+          if (lane == 0) ready = mbar_test_wait(smem_u32(done_full + slot), (dd / kDoneSlots) & 1);
+          if (__shfl_sync(kFullMask, ready ? 1 : 0, 0) == 0) break;
+          rec[i] = done_info[slot];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(done_empty + slot));
+          ++dd;
+          ++nrec;
+          if (rec[i].b < 0) consumers_done = true;
         }
+        if (nrec == 0) return;
         __threadfence();
-        if (lane < di.members) {
-          const int bm = di.b + lane;
-          bool split = true;
-          if (di.members > 1) {  // group members: only split sequences are merged
-            int L = p.context_lens[bm];
-            L = L < 0 ? 0 : (L > l_max ? l_max : L);
-            split = L > p.part_tokens;
+#pragma unroll
+        for (int i = 0; i < kDoneSlots; ++i) {
+          if (i < nrec && rec[i].b >= 0 && lane < rec[i].members) {
+            const int bm = rec[i].b + lane;
+            bool split = true;
+            if (rec[i].members > 1) {  // group members: only split sequences are merged
+              int L = p.context_lens[bm];
+              L = L < 0 ? 0 : (L > l_max ? l_max : L);
+              split = L > p.part_tokens;
+            }
+            if (split) atomicAdd(p.ws_count + static_cast<int64_t>(bm) * Z + rec[i].z, 1);
           }
-          if (split) atomicAdd(p.ws_count + static_cast<int64_t>(bm) * Z + di.z, 1);
         }
       }
     };
@@ -1218,11 +1227,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
   // fused step: once every CTA's partials are written, all warps of all CTAs
   // merge the split rows (one warp per query row)
   // Merge of split sequences, overlapped with other CTAs' decode: warp g of
-  // the launch takes rows g, g + (warps in the launch), ...; each row waits
-  // (bounded) until every unit of its (sequence, head tile) has been counted,
-  // then merges.  The last row of a (sequence, head tile) puts its two
-  // counters back to zero.  Every CTA is resident (cooperative launch), so
-  // the waits end.
+  // the launch takes rows g, g + (warps in the launch), ...; a row is merged
+  // once every unit of its (sequence, head tile) has been counted, rows of a
+  // warp in the order they become ready (bounded waits).  The last row of a
+  // (sequence, head tile) puts its two counters back to zero.  Every CTA is
+  // resident (cooperative launch), so the waits end.
   if ((flags & kOverlapCombine) && !failed) {
     const int nw = static_cast<int>(gridDim.x) * (W + 2);
     const int gwarp = static_cast<int>(blockIdx.x) * (W + 2) + warp;
@@ -1239,42 +1248,65 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       }
       pend_bz = -1;
     };
-    for (int row = gwarp; row < n_rows; row += nw) {
-      const int b = row / p.num_q_heads;
-      const int h = row - b * p.num_q_heads;
-      int L = p.context_lens[b];
-      L = L < 0 ? 0 : (L > l_max ? l_max : L);
-      const int n_parts = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-      if (n_parts < 2) continue;
-      const int kvh = h / p.group;
-      const int tile = (h - kvh * p.group) / HT;
-      const int bz = b * Z + kvh * p.num_head_tiles + tile;
-      const int nh_z = min(HT, p.group - tile * HT);
-      bool ready = true;
-      if (lane == 0) {
-        const uint64_t t0 = global_timer_ns();
-        while (true) {
+    // rows are taken kRowsAtOnce at a time (lane r holds row r) and merged in
+    // the order their sequences complete
+    constexpr int kRowsAtOnce = 8;
+    for (int row0 = gwarp; row0 < n_rows; row0 += kRowsAtOnce * nw) {
+      const int my_row = row0 + lane * nw;
+      const bool mine = lane < kRowsAtOnce && my_row < n_rows;
+      int my_np = 1, my_bz = 0, my_nh = 0;
+      if (mine) {
+        const int b = my_row / p.num_q_heads;
+        const int h = my_row - b * p.num_q_heads;
+        int L = p.context_lens[b];
+        L = L < 0 ? 0 : (L > l_max ? l_max : L);
+        my_np = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+        const int kvh = h / p.group;
+        const int tile = (h - kvh * p.group) / HT;
+        my_bz = b * Z + kvh * p.num_head_tiles + tile;
+        my_nh = min(HT, p.group - tile * HT);
+      }
+      unsigned pending = __ballot_sync(kFullMask, mine && my_np >= 2);
+      uint64_t t0 = 0;
+      if (lane == 0) t0 = global_timer_ns();
+      bool timed_out = false;
+      while (pending != 0) {
+        bool rdy = false;
+        if ((pending >> lane) & 1) {
           int c;
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(c) : "l"(count + bz) : "memory");
-          if (c >= n_parts) break;
-          if (global_timer_ns() - t0 > p.wait_limit_ns) {
-            ready = false;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(c) : "l"(count + my_bz) : "memory");
+          rdy = c >= my_np;
+        }
+        unsigned ready = __ballot_sync(kFullMask, rdy) & pending;
+        if (ready == 0) {
+          bool late = false;
+          if (lane == 0) late = global_timer_ns() - t0 > p.wait_limit_ns;
+          if (__shfl_sync(kFullMask, late ? 1 : 0, 0) != 0) {
+            timed_out = true;
             break;
           }
           __nanosleep(128);
+          continue;
+        }
+        __syncwarp();  // the ready lanes' acquires order every lane's partial loads below
+        pending &= ~ready;
+        while (ready != 0) {
+          const int r = __ffs(ready) - 1;
+          ready &= ready - 1;
+          const int rows1[1] = {__shfl_sync(kFullMask, my_row, r)};
+          const int bz = __shfl_sync(kFullMask, my_bz, r);
+          const int nh_z = __shfl_sync(kFullMask, my_nh, r);
+          combine_rows<T, D, 1>(p, rows1, lane);
+          settle();
+          if (lane == 0) pend_old = atomicAdd(rows_done + bz, 1);
+          pend_bz = bz;
+          pend_nh = nh_z;
         }
       }
-      if (__shfl_sync(kFullMask, ready ? 1 : 0, 0) == 0) {
+      if (timed_out) {
         if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
         break;
       }
-      __syncwarp();  // lane 0's acquire orders every lane's partial loads below
-      const int rows1[1] = {row};
-      combine_rows<T, D, 1>(p, rows1, lane);
-      settle();
-      if (lane == 0) pend_old = atomicAdd(rows_done + bz, 1);
-      pend_bz = bz;
-      pend_nh = nh_z;
     }
     settle();
   }

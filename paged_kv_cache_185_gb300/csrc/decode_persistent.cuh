@@ -92,10 +92,11 @@ constexpr int kMaxGroup = 8;
 // sequence order (decoded without a schedule, and a shared prompt prefix --
 // the first partitions -- is handed out early).  Phase B: the later
 // partitions except each sequence's last, sequence-major (prefix sums).
-// Phase C: each sequence's last partition when it lies beyond phase A, in
-// sequence order (ids of sequences without one decode to nothing).  The last
-// partitions are usually partial, so the units handed out last are short.
+// Phase C: each sequence's last partition when it lies beyond phase A,
+// longest first (32 length buckets, ties in sequence order), so the units
+// handed out last are the shortest.
 constexpr int kPhaseAParts = 2;
+constexpr int kOrderKeys = 36;  // phase-C length buckets 1..32 (0: no phase-C unit), padded
 
 constexpr int kSub = 4;                      // 16-token sub-chunks per stage
 constexpr int kStageTokens = kSub * kChunk;  // 64 tokens per stage
@@ -158,7 +159,9 @@ struct PShape {
   // multiple of 8 per thread)
   static constexpr int kMaxRegsRaw = 65536 / (kCtasPerSm * kThreads) / 8 * 8;
   static constexpr int kMaxRegs = kMaxRegsRaw > 255 ? 255 : kMaxRegsRaw;
-  static constexpr int kSeqBytes = ((kPersistentMaxSeqs + 1) * 4 + 15) / 16 * 16;
+  // prefix sums; phase-C bucket starts, order and keys
+  static constexpr int kSeqBytes = ((kPersistentMaxSeqs + 1) * 4 + 15) / 16 * 16 + kOrderKeys * 4 +
+                                   (kPersistentMaxSeqs * 3 + 15) / 16 * 16;
   static constexpr int kSmemPerCta = 233472 / kCtasPerSm - 1024;
   static constexpr int kQueueBytes =
       kQueue * (static_cast<int>(sizeof(Piece)) + 16) + kDoneSlots * (static_cast<int>(sizeof(DoneInfo)) + 16) + 16;
@@ -521,6 +524,9 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
   DoneInfo* done_info = reinterpret_cast<DoneInfo*>(pieces + kQueue);
   int* wsum = reinterpret_cast<int*>(done_info + kDoneSlots);  // 16 ints of scratch
   int* prefix = wsum + 16;                       // [B + 1] units before sequence b
+  int* order_cnt = prefix + ((p.num_seqs + 1 + 3) & ~3);                  // [kOrderKeys] bucket starts
+  uint16_t* order = reinterpret_cast<uint16_t*>(order_cnt + kOrderKeys);  // [B] phase-C sequences
+  uint8_t* okey = reinterpret_cast<uint8_t*>(order + p.num_seqs);         // [B] their buckets
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.num_seqs;
@@ -647,6 +653,43 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     };
     bool have_prefix = false;
     bool wait_ok = true;
+    // Phase-C order, built once by this warp right after the consumers'
+    // prefix pass (which also wrote each sequence's bucket): the sequences
+    // whose last partition lies past phase A, bucketed by that partition's
+    // length (32 buckets over P tokens), most first, ties in sequence order --
+    // a stable counting sort, 32 sequences at a time.  order_cnt[0] = their
+    // number.
+    auto build_order = [&]() {
+      for (int i = lane; i < kOrderKeys; i += 32) order_cnt[i] = 0;
+      __syncwarp();
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int k = b0 + lane < B ? okey[b0 + lane] : -1;
+        const unsigned same = __match_any_sync(kFullMask, k);
+        if (k > 0 && lane == __ffs(same) - 1) order_cnt[k] += __popc(same);
+        __syncwarp();
+      }
+      if (lane == 0) {  // bucket k starts after every bucket above it; [0] = total
+        int run = 0;
+        for (int k = 32; k >= 1; --k) {
+          const int c = order_cnt[k];
+          order_cnt[k] = run;
+          run += c;
+        }
+        order_cnt[0] = run;
+      }
+      __syncwarp();
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int k = b0 + lane < B ? okey[b0 + lane] : -1;
+        const unsigned same = __match_any_sync(kFullMask, k);
+        const int leader = __ffs(same) - 1;
+        int base = (lane == leader && k > 0) ? order_cnt[k] : 0;
+        base = __shfl_sync(kFullMask, base, leader);
+        if (k > 0) order[base + __popc(same & ((1u << lane) - 1u))] = static_cast<uint16_t>(b0 + lane);
+        __syncwarp();
+        if (lane == leader && k > 0) order_cnt[k] = base + __popc(same);
+        __syncwarp();
+      }
+    };
     // unit u -> (sequence, partition, kv-head tile) and the table entries of
     // its first 32 chunks (two per chunk when blocks hold 8 tokens).  Returns
     // false past the last unit.
@@ -689,21 +732,18 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
           wait_ok = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
           have_prefix = true;
           if (!wait_ok) return false;
+          build_order();
         }
         const int u2 = u - kPhaseAParts * BZ;
         if (u2 >= prefix[B]) {  // phase C
           const int u3 = u2 - prefix[B];
-          if (u3 >= BZ) return false;
-          x.b = u3 / Z;
-          x.z = u3 - x.b * Z;
+          if (u3 >= order_cnt[0] * Z) return false;
+          const int idx = u3 / Z;
+          x.b = order[idx];
+          x.z = u3 - idx * Z;
           L = p.context_lens[x.b];
           L = L < 0 ? 0 : (L > l_max ? l_max : L);
           const int np = (L + p.part_tokens - 1) / p.part_tokens;
-          if (np <= kPhaseAParts) {  // its last partition was in phase A
-            x.group = 0;
-            x.n_chunks = 0;
-            return true;
-          }
           x.part = np - 1;
           x.tb = x.part * p.part_tokens;
           x.te = L;
@@ -1023,7 +1063,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
 
   // ------------------------------- consumers --------------------------------
   // prefix sums of the phase-B units (partitions >= kPhaseAParts but the
-  // last), sequence-major; then tell the scheduler
+  // last), sequence-major, and the phase-C buckets; then tell the scheduler
   {
     constexpr int kCT = W * 32;
     const int per = (B + kCT - 1) / kCT;
@@ -1048,7 +1088,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       prefix[b] = run;
       int L = p.context_lens[b];
       L = L < 0 ? 0 : (L > l_max ? l_max : L);
-      run += max(0, (L + p.part_tokens - 1) / p.part_tokens - kPhaseAParts - 1) * Z;
+      const int np = (L + p.part_tokens - 1) / p.part_tokens;
+      run += max(0, np - kPhaseAParts - 1) * Z;
+      // phase-C bucket: length of the last partition in 32nds of P (0: none)
+      const int last = L - (np - 1) * p.part_tokens;
+      okey[b] = static_cast<uint8_t>(np <= kPhaseAParts ? 0 : min(32, (last * 32 + p.part_tokens - 1) / p.part_tokens));
     }
     if (threadIdx.x == kCT - 1) prefix[B] = wsum[0] + wsum[1] + wsum[2] + wsum[3];
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
@@ -1324,7 +1368,7 @@ __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
 
 template <typename T, int D, int NT>
 int persistent_smem(int num_seqs) {
-  return PShape<T, D, NT>::kFixedSmem + ((num_seqs + 1) * 4 + 15) / 16 * 16;
+  return PShape<T, D, NT>::kFixedSmem + ((num_seqs + 1 + 3) & ~3) * 4 + kOrderKeys * 4 + (num_seqs * 3 + 15) / 16 * 16;
 }
 
 // Launch the persistent decode.  `ap` non-null fuses the KV append in front of

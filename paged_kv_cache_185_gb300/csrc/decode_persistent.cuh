@@ -218,18 +218,12 @@ __device__ __forceinline__ bool consumer_sync(uint32_t bar, int& phase, uint64_t
 // all R rows when each has at most kBatch partitions: the context lengths,
 // then every (m, l) pair and partial at once.  rows[r] < 0 skips slot r; rows
 // with one partition were written by the decode itself.
+// The same with the rows' partition counts given (n[r] < 2 skips row r).
 template <typename T, int D, int R>
-__device__ __forceinline__ void combine_rows(const DecodeParams& p, const int (&rows)[R], int lane) {
+__device__ __forceinline__ void combine_rows_np(const DecodeParams& p, const int (&rows)[R], const int (&n)[R],
+                                                int lane) {
   constexpr int V = D / 32;
   constexpr int kBatch = 32 / V;
-  const int l_max = p.max_blocks * p.block_size;
-  int n[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    int L = rows[r] >= 0 ? p.context_lens[rows[r] / p.num_q_heads] : 0;
-    L = L < 0 ? 0 : (L > l_max ? l_max : L);
-    n[r] = (rows[r] < 0 || L == 0) ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-  }
   auto load_part = [&](const float* src, float* dst) {
     if constexpr (V >= 4) {
 #pragma unroll
@@ -308,6 +302,19 @@ __device__ __forceinline__ void combine_rows(const DecodeParams& p, const int (&
 #pragma unroll
     for (int i = 0; i < V; ++i) orow[i] = from_f32<T>(acc[i] * inv);
   }
+}
+
+template <typename T, int D, int R>
+__device__ __forceinline__ void combine_rows(const DecodeParams& p, const int (&rows)[R], int lane) {
+  const int l_max = p.max_blocks * p.block_size;
+  int n[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    int L = rows[r] >= 0 ? p.context_lens[rows[r] / p.num_q_heads] : 0;
+    L = L < 0 ? 0 : (L > l_max ? l_max : L);
+    n[r] = (rows[r] < 0 || L == 0) ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  }
+  combine_rows_np<T, D, R>(p, rows, n, lane);
 }
 
 // NS consecutive 16-token sub-chunks (sub-chunk j's K at k_base + j * kKV,
@@ -1295,6 +1302,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     // rows are taken kRowsAtOnce at a time (lane r holds row r) and merged in
     // the order their sequences complete
     constexpr int kRowsAtOnce = 8;
+    constexpr int kMergeBatch = 2;
     for (int row0 = gwarp; row0 < n_rows; row0 += kRowsAtOnce * nw) {
       const int my_row = row0 + lane * nw;
       const bool mine = lane < kRowsAtOnce && my_row < n_rows;
@@ -1334,17 +1342,27 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
         }
         __syncwarp();  // the ready lanes' acquires order every lane's partial loads below
         pending &= ~ready;
-        while (ready != 0) {
-          const int r = __ffs(ready) - 1;
-          ready &= ready - 1;
-          const int rows1[1] = {__shfl_sync(kFullMask, my_row, r)};
-          const int bz = __shfl_sync(kFullMask, my_bz, r);
-          const int nh_z = __shfl_sync(kFullMask, my_nh, r);
-          combine_rows<T, D, 1>(p, rows1, lane);
-          settle();
-          if (lane == 0) pend_old = atomicAdd(rows_done + bz, 1);
-          pend_bz = bz;
-          pend_nh = nh_z;
+        while (ready != 0) {  // up to kMergeBatch ready rows per batched load
+          int rows_b[kMergeBatch], np_b[kMergeBatch], bz_b[kMergeBatch], nh_b[kMergeBatch];
+#pragma unroll
+          for (int i = 0; i < kMergeBatch; ++i) {
+            const int r = ready != 0 ? __ffs(ready) - 1 : -1;
+            if (r >= 0) ready &= ready - 1;
+            const int rs = r >= 0 ? r : 0;
+            rows_b[i] = r >= 0 ? __shfl_sync(kFullMask, my_row, rs) : -1;
+            np_b[i] = r >= 0 ? __shfl_sync(kFullMask, my_np, rs) : 1;
+            bz_b[i] = __shfl_sync(kFullMask, my_bz, rs);
+            nh_b[i] = __shfl_sync(kFullMask, my_nh, rs);
+          }
+          combine_rows_np<T, D, kMergeBatch>(p, rows_b, np_b, lane);
+#pragma unroll
+          for (int i = 0; i < kMergeBatch; ++i) {
+            if (rows_b[i] < 0) break;
+            settle();
+            if (lane == 0) pend_old = atomicAdd(rows_done + bz_b[i], 1);
+            pend_bz = bz_b[i];
+            pend_nh = nh_b[i];
+          }
         }
       }
       if (timed_out) {

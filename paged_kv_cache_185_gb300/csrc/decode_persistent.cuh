@@ -2,36 +2,39 @@
 // f16/bf16 (tensor-core QK^T and PV), sm_103a.
 //
 // Work is cut into units (sequence b, kv-head tile z, partition p of P tokens).
-// The grid is a few CTAs per SM; each CTA loops until the units run out.
+// The grid is two CTAs per SM (one for head_dim 256); each CTA loops until the
+// units run out.  Six warps per CTA:
 //
-//   producer warp: takes the next unit from a device-wide atomic counter,
-//     loads that unit's block-table entries (32 chunks per coalesced load),
-//     and for every 16-token chunk waits for a free stage of the CTA's ring,
-//     writes the chunk's metadata, and issues 3-D TMA tiled copies of the 16
-//     K rows and 16 V rows of the kv head (128-byte swizzled); the first chunk
-//     of a unit also carries the unit's query rows (bulk copy).  It runs
-//     ahead across unit boundaries, so the copies of the next unit are in
-//     flight while the consumers finish the current one.
-//   consumer warps (4): a stage holds 64 tokens as four 16-token sub-chunks;
-//     consumer j takes sub-chunk j: S^T = K Q^T (mma.sync m16n8k16, the GQA
-//     heads of the tile on the N side), the online-softmax update and
-//     O^T += V^T P^T over the full head_dim, keeping its own running
-//     (m, l, O).  After the sub-chunk it releases the stage.
+//   scheduler warp: claims units (CTA i starts with unit i, the rest come
+//     from a device-wide atomic counter), decodes them, loads their
+//     block-table entries (32 chunks per coalesced load), detects prefix
+//     groups, and hands the producer pieces of up to 32 chunks through a
+//     small shared-memory queue.  It also counts finished units of split
+//     sequences (below).
+//   producer warp: for every 64-token stage of a piece waits for a free slot
+//     of the CTA's ring, writes the stage record, and issues 3-D TMA tiled
+//     copies of the 4 x 16 K rows and 4 x 16 V rows of the kv head (128-byte
+//     swizzled); a unit's first stage also carries its query rows (bulk copy).
+//   consumer warps (4): consumer j takes 16-token sub-chunk j of each stage:
+//     S^T = K Q^T (mma.sync m16n8k16, the GQA heads of the tile on the N
+//     side), the online-softmax update and O^T += V^T P^T over the full
+//     head_dim, keeping its own running (m, l, O).  A prefix-group unit is
+//     instead consumed two member sequences per warp over whole stages.
 //
-// At the end of a unit the consumers merge their four (m, l, O) through
-// shared memory (two rendezvous on a bounded mbarrier).  A sequence with one
-// partition gets its output written there; otherwise the merged partial goes
-// to the workspace and a combine kernel, launched right after, merges the
-// partitions (so no consumer ever waits on a fence or an atomic).
+// At the end of a unit the consumers merge their four (m, l, O) in the ring
+// slot of the unit's last stage.  A sequence with one partition gets its
+// output written there; otherwise the partial goes to the workspace, the
+// scheduler warp counts it, and after its own work every warp of the launch
+// merges the rows whose sequences are complete (counters, bounded polling).
 //
-// Unit order: first every (sequence, kv-head tile) at partition 0 -- CTA i
-// starts on unit i at once, needing only sequence i / Z's length and table
-// row, while the consumer warps build the prefix sums that map the later
-// units (partitions >= 1, sequence-major) -- then the rest from the counter.
+// Unit order: partitions 0 and 1 of every sequence, partition-major (no
+// schedule needed, shared prefixes first); then the remaining partitions but
+// each sequence's last, sequence-major (prefix sums built by the consumer
+// warps at launch start); then the last partitions, longest first.
 //
 // Every wait is bounded: on timeout the warp records an error bit and leaves.
-// The scheduler counter is reset by the last CTA to finish, so it is zero
-// between launches.
+// The scheduler counters and the merge counters are left at zero by every
+// launch.
 #pragma once
 
 #include "append_row.cuh"
@@ -99,7 +102,6 @@ constexpr int kPhaseAParts = 2;
 constexpr int kOrderKeys = 36;  // phase-C length buckets 1..32 (0: no phase-C unit), padded
 
 constexpr int kSub = 4;                      // 16-token sub-chunks per stage
-constexpr int kStageTokens = kSub * kChunk;  // 64 tokens per stage
 
 // One unit of work: query heads h0 .. h0+nh-1 (kv head kvh, head tile z) of
 // sequence b over tokens [tb, te) of partition `part`.

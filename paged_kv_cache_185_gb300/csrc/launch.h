@@ -24,7 +24,8 @@ struct DecodeParams {
   float scale_log2;               // scale * log2(e)
   float* ws_o;                    // [B*Hq][max_parts][D] unnormalised partial sums
   float* ws_ml;                   // [B*Hq][max_parts][2] running max (log2 units), sum
-  int* ws_count;                  // [B*Hkv*num_head_tiles] arrival counters, zero between calls
+  int* ws_count;                  // counters, zero between calls: grid kernel [B*Hkv*tiles] arrivals;
+                                  // persistent kernel [2][B*Hkv*tiles] units finished, rows merged
   int* err;                       // device error word
   unsigned long long wait_limit_ns;
   int prefix_groups;              // process shared-prefix partitions once per group of sequences
@@ -59,9 +60,10 @@ int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& k
 
 // Persistent warp-specialised decode (f16/bf16 only).  `separate_combine`
 // appends the split-KV combine kernel (needed when a sequence can span
-// several partitions).
-// `ap` (may be null) fuses the KV append in front; `fuse_combine` merges the
-// partitions inside the launch (both make it a cooperative launch).
+// several partitions and `fuse_combine` is not set).  `ap` (may be null)
+// fuses the KV append in front; `fuse_combine` merges the partitions inside
+// the launch, as they complete (p.ws_count must then hold the zeroed
+// counters).  Either makes it a cooperative launch.
 int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
                              const AppendParams* ap, bool fuse_combine, cudaStream_t stream);

@@ -52,6 +52,56 @@ WORKLOAD_DESC = {
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 
 
+def graph_layers(args, case, dev, q, key, value, slots, bt, cl, flush, stream):
+    """Several layers' decode steps (each layer its own K/V pools, the same step
+    inputs) back to back, issued eagerly and replayed from one CUDA graph; the
+    L2 is flushed between repetitions, outside the events.  Returns per-layer
+    times, or None when the layers' pools would not fit the budget."""
+    import paged_kv_cache_185_gb300 as wllm
+
+    L = args.graph_layers
+    if L <= 0 or L * 2 * case.pool_bytes() > (8 << 30) or case.dtype == torch.float32:
+        return None
+    B, Hq, Hkv, D, bs = case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
+    pools = [case.pool(dev) for _ in range(L)]
+    outs = [torch.empty_like(q) for _ in range(L)]
+    need = wllm.workspace_bytes(B, Hq, Hkv, D, case.max_blocks, bs)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    wllm.set_workspace(ws)
+    try:
+        def layers():
+            for (kc, vc), o in zip(pools, outs):
+                wllm.decode_step(o, q, key, value, kc, vc, slots, bt, cl, Hkv, case.scale, bs)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                layers()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layers()
+        torch.cuda.synchronize()
+        R = max(20, min(args.steps, 200))
+        res = {}
+        for name, fn in (("eager", layers), ("graph", g.replay)):
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+            for e in ev:
+                flush.zero_()
+                e[0].record(stream)
+                fn()
+                e[1].record(stream)
+            torch.cuda.synchronize()
+            res[name] = sum(e[0].elapsed_time(e[1]) for e in ev) / R * 1e3 / L
+        return {"layers": L, "us_per_layer": res["graph"], "eager_us_per_layer": res["eager"],
+                "note": "layers back to back, each on its own K/V pools; one CUDA graph replay vs eager calls"}
+    finally:
+        wllm.set_workspace(None)
+        del pools
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -342,6 +392,8 @@ def run_ours(args):
     e2e_ms = all_max(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / K, world)
     e2e_value = B * world / (e2e_ms / 1e3)
 
+    graph = graph_layers(args, case, dev, q, key, value, slots, bt, cl, flush, stream)
+
     peak, peak_kind = measured_peak()
     alg = case.algorithmic_bytes()
     dec_mean = sum(dec_ms) / len(dec_ms)
@@ -373,6 +425,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks.summary(),
+        "graph": graph,
     }
     print(json.dumps(line), flush=True)
 
@@ -382,6 +435,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--graph-layers", type=int, default=8,
+                    help="layers per CUDA-graph replay for the graph measurement (0: skip)")
     ap.add_argument("--workload", default="c1", choices=list(workloads.CASE_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -133,9 +133,12 @@ int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value,
  * fp32 accumulation; F32 uses fp32 FMA.  The cache base pointers must be
  * 16-byte aligned.  Long contexts are split over several CTAs and combined on
  * the device (split-KV); this uses the device workspace (see below).  With
- * F16/BF16 the partitions are merged inside one cooperative launch (every CTA
- * resident; grid barriers bounded in time), or by a second kernel when the
- * environment variable WLLM_SEPARATE_COMBINE=1 is set.
+ * F16/BF16 the partitions of a sequence are merged inside the same
+ * (cooperative) launch as soon as all of them are done -- per-sequence
+ * counters in the workspace, waits bounded in time -- or by a second kernel
+ * when the environment variable WLLM_SEPARATE_COMBINE=1 is set.  With a
+ * caller workspace set (wllm_set_workspace) the call allocates nothing and can
+ * be captured in a CUDA graph.
  * A block-table entry outside [0, N_b) or a length above M_b*bs is clamped on
  * the device (the output of that sequence is then meaningless) and, in check
  * mode, reported as WLLM_ERR_OUT_OF_RANGE.
@@ -161,9 +164,11 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q,
  * the same as calling the two in order: every appended row is visible to the
  * attention.  For F16/BF16 with 16-byte aligned query rows it is one
  * cooperative launch of the persistent kernel: its CTAs append their share of
- * the rows, meet at a grid barrier, attend, and -- when sequences are split --
- * meet again and merge the partitions.  Other inputs run the two calls' kernels
- * back to back.  T == 0 skips the append; B == 0 skips the attention.
+ * the rows, meet at a bounded grid barrier, then attend, split sequences being
+ * merged as in wllm_paged_attention_decode.  Other inputs run the two calls'
+ * kernels back to back.  T == 0 skips the append; B == 0 skips the attention.
+ * With a caller workspace set the step allocates nothing, so a model's layers
+ * can be captured once in a CUDA graph and replayed.
  */
 int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key,
                      const wllm_tensor* value, const wllm_tensor* k_cache, const wllm_tensor* v_cache,
@@ -209,7 +214,10 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
 /*
  * Bytes of device workspace that wllm_paged_attention_decode needs for these
  * sizes (0 when no sequence is split).  The workspace holds the split-KV
- * partial results and one arrival counter per (sequence, kv head, head tile).
+ * partial results and two counters per (sequence, kv head, head tile) for the
+ * merge inside the launch.  Every launch leaves the counters at zero; after a
+ * launch reports a timed-out wait (error bit 4), wllm_device_errors() zeroes
+ * them again.
  */
 size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                             int head_dim, int max_blocks_per_seq,

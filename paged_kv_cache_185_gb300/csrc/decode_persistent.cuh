@@ -1420,13 +1420,19 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
   if (flags == 0) {
     kernel<<<grid, PS::kThreads, smem, stream>>>(kmap, vmap, p, app, flags);
   } else {
-    CUtensorMap km = kmap, vm = vmap;
-    DecodeParams pp = p;
-    AppendParams aa = app;
-    int ff = flags;
-    void* args[] = {&km, &vm, &pp, &aa, &ff};
-    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(PS::kThreads), args,
-                                    smem, stream);
+    // cooperative (every CTA resident), through the extensible launch so that
+    // stream capture records it as a cooperative kernel node
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(PS::kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p, app, flags);
     if (e != cudaSuccess) return e;
   }
   e = cudaGetLastError();

@@ -257,6 +257,79 @@ const char* wllm_last_error(void);
 /* Library version string. */
 const char* wllm_version(void);
 
+/* ---------------------------------------------------------------------------
+ * Prefix-caching block manager (host side).
+ *
+ * Passages: "wLLM" project page, "Features / Core engine" (block-based KV
+ * cache; prefix sharing is a block-table operation); "mini-vLLM" README,
+ * "How it works / Paged KV-cache" and "What changed" (block tables, a
+ * reference count reserved per block for sharing).
+ *
+ * Decides which physical block of a pool of num_blocks blocks of block_size
+ * token slots holds which tokens of which sequence, and produces the block
+ * tables, context lengths and slot mappings the calls above consume.  A full
+ * block is identified by the chain hash of all tokens up to its last one and
+ * keeps its tokens (a hit is checked token for token); sequences whose prompts
+ * share full leading blocks share those physical blocks.  Each block counts
+ * the sequences that name it; writing into a block that others also name
+ * first moves the writer to a private copy (copy-on-write, reported to the
+ * caller, who copies the slots on the device).  Unreferenced full blocks stay
+ * cached, evictable least recently freed first; other free blocks are used
+ * first.  A manager is not thread-safe.  Calls that fail leave it unchanged:
+ * WLLM_ERR_INVALID_ARG for unknown or duplicate sequence ids and bad
+ * arguments, WLLM_ERR_OUT_OF_RANGE when the pool has too few free blocks (or a
+ * table row is too short).  All pointers are host pointers owned by the
+ * caller.
+ * ------------------------------------------------------------------------- */
+typedef struct wllm_block_manager wllm_block_manager;
+
+/* New manager over blocks 0 .. num_blocks-1 (block 0 is handed out first). */
+int wllm_bm_create(int num_blocks, int block_size, wllm_block_manager** out);
+void wllm_bm_destroy(wllm_block_manager* bm);
+
+/*
+ * Register sequence seq_id with its n prompt tokens.  Leading full blocks
+ * already cached with the same tokens are shared; the rest are fresh blocks.
+ * slots (may be NULL) receives [n] the slot (block * block_size + offset) of
+ * every token; *cached_tokens (may be NULL) the number of leading tokens whose
+ * K/V is already in the cache (a multiple of block_size): only slots from
+ * there on need writing.
+ */
+int wllm_bm_add_sequence(wllm_block_manager* bm, int64_t seq_id, const int32_t* tokens, int64_t n,
+                         int64_t* slots, int64_t* cached_tokens);
+
+/*
+ * Append one token to seq_id (a decode step): *slot receives the slot the
+ * token's K/V goes to.  If the sequence's last block was shared and partly
+ * filled, the sequence first moves to a private copy: *copy_src / *copy_dst
+ * receive the two blocks and the caller must copy the first
+ * (context_len % block_size) slots of each kv head from src to dst before
+ * writing; otherwise both receive -1.  A block that becomes full is cached.
+ */
+int wllm_bm_append_token(wllm_block_manager* bm, int64_t seq_id, int32_t token, int64_t* slot,
+                         int32_t* copy_src, int32_t* copy_dst);
+
+/* child shares all of parent's blocks (e.g. several samples of one prompt). */
+int wllm_bm_fork(wllm_block_manager* bm, int64_t parent, int64_t child);
+
+/* Drop seq_id; blocks no longer named by any sequence become free. */
+int wllm_bm_free_sequence(wllm_block_manager* bm, int64_t seq_id);
+
+/*
+ * seq_id's block-table row: row[0 .. max_blocks) gets its blocks, -1 past the
+ * last; *context_len (may be NULL) its token count.  WLLM_ERR_OUT_OF_RANGE if
+ * the sequence holds more than max_blocks blocks.
+ */
+int wllm_bm_block_table(const wllm_block_manager* bm, int64_t seq_id, int32_t* row, int max_blocks,
+                        int64_t* context_len);
+
+/* Free blocks (unreferenced, cached ones included); -1 for a NULL manager. */
+int64_t wllm_bm_num_free_blocks(const wllm_block_manager* bm);
+/* Full blocks currently findable by prompt tokens; -1 for a NULL manager. */
+int64_t wllm_bm_num_cached_blocks(const wllm_block_manager* bm);
+/* Sequences naming block (its reference count); -1 if out of range. */
+int wllm_bm_block_ref(const wllm_block_manager* bm, int32_t block);
+
 #ifdef __cplusplus
 }
 #endif

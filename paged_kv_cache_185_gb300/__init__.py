@@ -14,7 +14,7 @@ from __future__ import annotations
 __all__ = ["reshape_and_cache", "paged_attention_decode", "paged_attention_decode_noalloc",
            "workspace_bytes", "set_workspace",
            "partition_tokens", "device_errors", "version", "load_library",
-           "decode_step", "WllmError", "library_path"]
+           "decode_step", "WllmError", "library_path", "BlockManager"]
 
 
 def __getattr__(name):

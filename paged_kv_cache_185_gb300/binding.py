@@ -24,7 +24,10 @@ _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3,
 EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode", "wllm_decode_step",
             "wllm_paged_attention_decode_noalloc",
             "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
-            "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version")
+            "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version",
+            "wllm_bm_create", "wllm_bm_destroy", "wllm_bm_add_sequence", "wllm_bm_append_token",
+            "wllm_bm_fork", "wllm_bm_free_sequence", "wllm_bm_block_table", "wllm_bm_num_free_blocks",
+            "wllm_bm_num_cached_blocks", "wllm_bm_block_ref")
 
 
 class WllmError(RuntimeError):
@@ -81,6 +84,28 @@ def load_library():
         lib.wllm_last_error.restype = ctypes.c_char_p
         lib.wllm_version.argtypes = []
         lib.wllm_version.restype = ctypes.c_char_p
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        p64, p32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+        lib.wllm_bm_create.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)]
+        lib.wllm_bm_create.restype = ctypes.c_int
+        lib.wllm_bm_destroy.argtypes = [vp]
+        lib.wllm_bm_destroy.restype = None
+        lib.wllm_bm_add_sequence.argtypes = [vp, i64, p32, i64, p64, p64]
+        lib.wllm_bm_add_sequence.restype = ctypes.c_int
+        lib.wllm_bm_append_token.argtypes = [vp, i64, i32, p64, p32, p32]
+        lib.wllm_bm_append_token.restype = ctypes.c_int
+        lib.wllm_bm_fork.argtypes = [vp, i64, i64]
+        lib.wllm_bm_fork.restype = ctypes.c_int
+        lib.wllm_bm_free_sequence.argtypes = [vp, i64]
+        lib.wllm_bm_free_sequence.restype = ctypes.c_int
+        lib.wllm_bm_block_table.argtypes = [vp, i64, p32, ctypes.c_int, p64]
+        lib.wllm_bm_block_table.restype = ctypes.c_int
+        lib.wllm_bm_num_free_blocks.argtypes = [vp]
+        lib.wllm_bm_num_free_blocks.restype = i64
+        lib.wllm_bm_num_cached_blocks.argtypes = [vp]
+        lib.wllm_bm_num_cached_blocks.restype = i64
+        lib.wllm_bm_block_ref.argtypes = [vp, i32]
+        lib.wllm_bm_block_ref.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -193,3 +218,76 @@ def device_errors() -> int:
 
 def version() -> str:
     return load_library().wllm_version().decode()
+
+
+class BlockManager:
+    """Prefix-caching manager of the physical KV blocks (host side; see the
+    wllm_bm_* calls in wllm.h).  Argument marshalling only."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        rc = self._lib.wllm_bm_create(int(num_blocks), int(block_size), ctypes.byref(h))
+        if rc != WLLM_OK:
+            raise WllmError(rc, "wllm_bm_create")
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if self._h:
+            self._lib.wllm_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _ok(rc: int, what: str):
+        if rc != WLLM_OK:
+            raise WllmError(rc, what)
+
+    def add_sequence(self, seq_id: int, tokens):
+        """Returns (slots [n] int64 tensor, number of leading tokens already cached)."""
+        t = torch.as_tensor(tokens, dtype=torch.int32).contiguous()
+        n = t.numel()
+        slots = torch.empty(n, dtype=torch.int64)
+        cached = ctypes.c_int64()
+        self._ok(self._lib.wllm_bm_add_sequence(
+            self._h, int(seq_id), ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_int32)) if n else None, n,
+            ctypes.cast(slots.data_ptr(), ctypes.POINTER(ctypes.c_int64)) if n else None, ctypes.byref(cached)),
+            "wllm_bm_add_sequence")
+        return slots, int(cached.value)
+
+    def append_token(self, seq_id: int, token: int):
+        """Returns (slot, copy) with copy = (src_block, dst_block) or None."""
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        self._ok(self._lib.wllm_bm_append_token(self._h, int(seq_id), int(token), ctypes.byref(slot),
+                                                ctypes.byref(src), ctypes.byref(dst)), "wllm_bm_append_token")
+        return int(slot.value), (None if src.value < 0 else (int(src.value), int(dst.value)))
+
+    def fork(self, parent: int, child: int):
+        self._ok(self._lib.wllm_bm_fork(self._h, int(parent), int(child)), "wllm_bm_fork")
+
+    def free_sequence(self, seq_id: int):
+        self._ok(self._lib.wllm_bm_free_sequence(self._h, int(seq_id)), "wllm_bm_free_sequence")
+
+    def block_table(self, seq_id: int, max_blocks: int):
+        """Returns (row [max_blocks] int32 tensor, -1 past the last block; context length)."""
+        row = torch.empty(int(max_blocks), dtype=torch.int32)
+        n = ctypes.c_int64()
+        self._ok(self._lib.wllm_bm_block_table(
+            self._h, int(seq_id), ctypes.cast(row.data_ptr(), ctypes.POINTER(ctypes.c_int32)) if max_blocks else None,
+            int(max_blocks), ctypes.byref(n)), "wllm_bm_block_table")
+        return row, int(n.value)
+
+    def num_free_blocks(self) -> int:
+        return int(self._lib.wllm_bm_num_free_blocks(self._h))
+
+    def num_cached_blocks(self) -> int:
+        return int(self._lib.wllm_bm_num_cached_blocks(self._h))
+
+    def block_ref(self, block: int) -> int:
+        return int(self._lib.wllm_bm_block_ref(self._h, int(block)))

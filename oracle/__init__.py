@@ -39,7 +39,7 @@ _LIB = os.path.join(_HERE, "_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
 _DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 _ERRORS = {
@@ -85,6 +85,15 @@ def _load():
             vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
             ctypes.c_float, i32, i32]
         lib.oracle_paged_decode_rows.restype = i32
+        lib.oracle_paged_decode_rows_kv.argtypes = [
+            vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+            ctypes.c_float, i32, i32, ctypes.c_float, ctypes.c_float, i32]
+        lib.oracle_paged_decode_rows_kv.restype = i32
+        lib.oracle_e4m3_encode.argtypes = [vp, vp, i64]
+        lib.oracle_e4m3_encode.restype = i32
+        lib.oracle_reshape_and_cache_e4m3.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
+                                                      ctypes.c_float, ctypes.c_float]
+        lib.oracle_reshape_and_cache_e4m3.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -116,6 +125,47 @@ def widen(x: torch.Tensor) -> torch.Tensor:
     return out
 
 
+def widen_e4m3(codes: torch.Tensor) -> torch.Tensor:
+    """Decode E4M3 codes (uint8) to float64 with the oracle's own decoder."""
+    codes = _host(codes, torch.uint8)
+    out = torch.empty(codes.shape, dtype=torch.float64)
+    _check(_load().oracle_widen(codes.data_ptr(), out.data_ptr(), codes.numel(), E4M3))
+    return out
+
+
+def e4m3_encode(x: torch.Tensor) -> torch.Tensor:
+    """Round float32 values to E4M3 codes (nearest, ties to even, saturating at +-448)."""
+    x = _host(x, torch.float32)
+    out = torch.empty(x.shape, dtype=torch.uint8)
+    _check(_load().oracle_e4m3_encode(x.data_ptr(), out.data_ptr(), x.numel()))
+    return out
+
+
+def inv_scale(scale: float) -> float:
+    """The binary32 reciprocal 1/scale that the FP8 append multiplies by."""
+    import numpy as np
+    return float(np.float32(1.0) / np.float32(scale))
+
+
+def reshape_and_cache_e4m3(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                           v_scale: float) -> None:
+    """In-place KV append into E4M3 caches (uint8 [N_b,Hkv,bs,D]): every element x is
+    stored as E4M3(fp32(x) * fp32(1/scale))."""
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    key, value = _host(key), _host(value)
+    kc, vc = _host(k_cache, torch.uint8), _host(v_cache, torch.uint8)
+    slots = _host(slot_mapping, torch.int64)
+    T, Hkv, D = key.shape
+    N_b, Hkv2, bs, D2 = kc.shape
+    if value.shape != key.shape or vc.shape != kc.shape or (Hkv2, D2) != (Hkv, D) or value.dtype != key.dtype:
+        raise ValueError("shape mismatch")
+    _check(_load().oracle_reshape_and_cache_e4m3(
+        key.data_ptr(), value.data_ptr(), kc.data_ptr(), vc.data_ptr(), slots.data_ptr(), T, Hkv, D, N_b, bs,
+        _DTYPE_CODE[key.dtype], inv_scale(k_scale), inv_scale(v_scale)))
+
+
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
                       v_cache: torch.Tensor, slot_mapping: torch.Tensor) -> None:
     """In-place KV append on host tensors: key/value [T,Hkv,D], caches [N_b,Hkv,bs,D]."""
@@ -136,12 +186,15 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
 
 def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
-                 scale: float, rows=None, num_threads: int = 0) -> torch.Tensor:
+                 scale: float, rows=None, num_threads: int = 0, k_scale: float = 1.0,
+                 v_scale: float = 1.0) -> torch.Tensor:
     """Paged decode attention in float64.
 
-    q [B,Hq,D]; caches [N_b,Hkv,bs,D]; block_tables int32 [B,M_b]; context_lens
-    int32 [B].  Returns float64 [B,Hq,D], or [len(rows),D] for the flat row
-    indices ``rows`` (r = b*Hq + h).  ``scale`` is used as its binary32 value.
+    q [B,Hq,D]; caches [N_b,Hkv,bs,D] of q's dtype, or uint8 E4M3 codes whose
+    values are code * k_scale (resp. v_scale); block_tables int32 [B,M_b];
+    context_lens int32 [B].  Returns float64 [B,Hq,D], or [len(rows),D] for the
+    flat row indices ``rows`` (r = b*Hq + h).  ``scale`` and the K/V scales are
+    used as their binary32 values.
     """
     q = _host(q)
     kc, vc = _host(k_cache), _host(v_cache)
@@ -151,7 +204,8 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     N_b, Hkv, bs, D2 = kc.shape
     if Hkv != num_kv_heads or D2 != D or vc.shape != kc.shape:
         raise ValueError("shape mismatch")
-    if not (q.dtype == kc.dtype == vc.dtype):
+    fp8 = kc.dtype == torch.uint8
+    if vc.dtype != kc.dtype or not (fp8 or q.dtype == kc.dtype):
         raise ValueError("dtype mismatch")
     if bt.dim() != 2 or bt.shape[0] != B or cl.shape != (B,):
         raise ValueError("block_tables/context_lens shape mismatch")
@@ -164,8 +218,9 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         rows_t = torch.as_tensor(rows, dtype=torch.int64).contiguous()
         n_rows = rows_t.numel()
         out = torch.empty((n_rows, D), dtype=torch.float64)
-    _check(_load().oracle_paged_decode_rows(
+    _check(_load().oracle_paged_decode_rows_kv(
         out.data_ptr(), None if rows_t is None else rows_t.data_ptr(), n_rows,
         q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), cl.data_ptr(),
-        B, Hq, Hkv, D, N_b, bs, M_b, float(scale), _DTYPE_CODE[q.dtype], int(num_threads)))
+        B, Hq, Hkv, D, N_b, bs, M_b, float(scale), _DTYPE_CODE[q.dtype], E4M3 if fp8 else _DTYPE_CODE[q.dtype],
+        float(k_scale) if fp8 else 1.0, float(v_scale) if fp8 else 1.0, int(num_threads)))
     return out

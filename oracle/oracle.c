@@ -56,7 +56,7 @@
 #endif
 
 /* element type codes used by the Python wrapper */
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_E4M3 = 3 };
 
 /* status codes */
 enum {
@@ -93,7 +93,47 @@ static double bf16_to_double(uint16_t b) {
   return (double)f;
 }
 
+/* OCP FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits; no infinities; exponent and fraction all ones is NaN; largest finite
+ * magnitude 448. */
+static double e4m3_to_double(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int e = (c >> 3) & 0xf;
+  int f = c & 7;
+  double v;
+  if (e == 15 && f == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f, -9); /* subnormal: f * 2^(1-7-3) */
+  } else {
+    v = ldexp((double)(f + 8), e - 10); /* (1 + f/8) * 2^(e-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round y to E4M3: the nearest finite code, ties to the code with an even
+ * fraction; magnitudes beyond the largest finite value give +-448
+ * (saturation); NaN gives NaN.  Written as a search over the 127 finite
+ * non-negative codes, which is slow and plainly the definition. */
+static uint8_t double_to_e4m3(double y) {
+  if (isnan(y)) return 0x7f;
+  const uint8_t sign = (y < 0 || (y == 0 && signbit(y))) ? 0x80 : 0;
+  const double a = fabs(y);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+  uint8_t best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7e; ++c) {
+    const double d = fabs(e4m3_to_double((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best_d = d;
+      best = (uint8_t)c;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
 static double load_elt(const void* base, int64_t i, int dtype) {
+  if (dtype == ORACLE_E4M3) return e4m3_to_double(((const uint8_t*)base)[i]);
   if (dtype == ORACLE_F32) {
     float f;
     memcpy(&f, (const char*)base + 4 * i, 4);
@@ -106,6 +146,7 @@ static double load_elt(const void* base, int64_t i, int dtype) {
 
 static int elt_bytes(int dtype) {
   switch (dtype) {
+    case ORACLE_E4M3: return 1;
     case ORACLE_F32: return 4;
     case ORACLE_F16:
     case ORACLE_BF16: return 2;
@@ -118,6 +159,51 @@ static int elt_bytes(int dtype) {
 int oracle_widen(const void* src, double* dst, int64_t n, int dtype) {
   if (elt_bytes(dtype) == 0) return ORACLE_BAD_DTYPE;
   for (int64_t i = 0; i < n; ++i) dst[i] = load_elt(src, i, dtype);
+  return ORACLE_OK;
+}
+
+/* Encode n binary32 values to E4M3 codes (exported so the tests can pin the
+ * rounding against an independent library conversion). */
+int oracle_e4m3_encode(const float* src, uint8_t* dst, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = double_to_e4m3((double)src[i]);
+  return ORACLE_OK;
+}
+
+/*
+ * KV-cache append into an FP8 (E4M3) cache with per-tensor scales.
+ * key, value: [T][Hkv][D] dense, dtype f32/f16/bf16.  k_cache, v_cache:
+ * [num_blocks][Hkv][block_size][D] bytes.  Every element x of key[t][h] is
+ * stored as E4M3(fp32(x) * k_inv_scale) -- the product taken in binary32 --
+ * in slot slot_mapping[t], and likewise for value with v_inv_scale.  Negative
+ * slots write nothing; an out-of-range slot writes nothing and returns
+ * ORACLE_SLOT_OUT_OF_RANGE.
+ */
+int oracle_reshape_and_cache_e4m3(const void* key, const void* value, uint8_t* k_cache, uint8_t* v_cache,
+                                  const int64_t* slot_mapping, int64_t num_tokens, int64_t num_kv_heads,
+                                  int64_t head_dim, int64_t num_blocks, int64_t block_size, int dtype,
+                                  float k_inv_scale, float v_inv_scale) {
+  if (elt_bytes(dtype) == 0 || dtype == ORACLE_E4M3) return ORACLE_BAD_DTYPE;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0 || block_size <= 0)
+    return ORACLE_BAD_SHAPE;
+  for (int64_t t = 0; t < num_tokens; ++t)
+    if (slot_mapping[t] >= num_blocks * block_size) return ORACLE_SLOT_OUT_OF_RANGE;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    const int64_t blk = s / block_size, off = s % block_size;
+    for (int64_t h = 0; h < num_kv_heads; ++h) {
+      const int64_t src = (t * num_kv_heads + h) * head_dim;
+      const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * head_dim;
+      for (int64_t d = 0; d < head_dim; ++d) {
+        const float xk = (float)load_elt(key, src + d, dtype);
+        const float xv = (float)load_elt(value, src + d, dtype);
+        const float yk = xk * k_inv_scale;
+        const float yv = xv * v_inv_scale;
+        k_cache[dst + d] = double_to_e4m3((double)yk);
+        v_cache[dst + d] = double_to_e4m3((double)yv);
+      }
+    }
+  }
   return ORACLE_OK;
 }
 
@@ -173,15 +259,17 @@ int oracle_reshape_and_cache(const void* key, const void* value, void* k_cache,
  * out[b][h][:] = (sum_j w_j V_j[:]) / (sum_j w_j).
  * L == 0 gives zeros.  Inputs are validated first; nothing is written on error.
  */
-int oracle_paged_decode_rows(double* out, const int64_t* rows, int64_t n_rows,
-                             const void* q, const void* k_cache,
-                             const void* v_cache, const int32_t* block_tables,
-                             const int32_t* context_lens, int64_t num_seqs,
-                             int64_t num_q_heads, int64_t num_kv_heads,
-                             int64_t head_dim, int64_t num_blocks,
-                             int64_t block_size, int64_t max_blocks,
-                             float scale, int dtype, int num_threads) {
-  if (elt_bytes(dtype) == 0) return ORACLE_BAD_DTYPE;
+int oracle_paged_decode_rows_kv(double* out, const int64_t* rows, int64_t n_rows,
+                                const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, int64_t num_seqs,
+                                int64_t num_q_heads, int64_t num_kv_heads,
+                                int64_t head_dim, int64_t num_blocks,
+                                int64_t block_size, int64_t max_blocks,
+                                float scale, int dtype, int kv_dtype, float k_scale,
+                                float v_scale, int num_threads) {
+  if (elt_bytes(dtype) == 0 || dtype == ORACLE_E4M3 || elt_bytes(kv_dtype) == 0) return ORACLE_BAD_DTYPE;
+  const double ks = (double)k_scale, vs = (double)v_scale;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || max_blocks < 0 || num_q_heads % num_kv_heads != 0)
     return ORACLE_BAD_SHAPE;
@@ -232,7 +320,7 @@ int oracle_paged_decode_rows(double* out, const int64_t* rows, int64_t n_rows,
       const int64_t k_off = ((pb * num_kv_heads + c) * block_size + j % block_size) * head_dim;
       double dot = 0.0;
       for (int64_t d = 0; d < head_dim; ++d)
-        dot += load_elt(q, q_off + d, dtype) * load_elt(k_cache, k_off + d, dtype);
+        dot += load_elt(q, q_off + d, dtype) * (load_elt(k_cache, k_off + d, kv_dtype) * ks);
       s[j] = scale_d * dot;
     }
     double m = s[0];
@@ -246,12 +334,25 @@ int oracle_paged_decode_rows(double* out, const int64_t* rows, int64_t n_rows,
       denom += w;
       const int64_t pb = block_tables[b * max_blocks + j / block_size];
       const int64_t v_off = ((pb * num_kv_heads + c) * block_size + j % block_size) * head_dim;
-      for (int64_t d = 0; d < head_dim; ++d) o[d] += w * load_elt(v_cache, v_off + d, dtype);
+      for (int64_t d = 0; d < head_dim; ++d) o[d] += w * (load_elt(v_cache, v_off + d, kv_dtype) * vs);
     }
     for (int64_t d = 0; d < head_dim; ++d) o[d] /= denom;
     free(s);
   }
   return status;
+}
+
+/* The same with K/V stored like q (scales 1). */
+int oracle_paged_decode_rows(double* out, const int64_t* rows, int64_t n_rows, const void* q,
+                             const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                             const int32_t* context_lens, int64_t num_seqs, int64_t num_q_heads,
+                             int64_t num_kv_heads, int64_t head_dim, int64_t num_blocks,
+                             int64_t block_size, int64_t max_blocks, float scale, int dtype,
+                             int num_threads) {
+  return oracle_paged_decode_rows_kv(out, rows, n_rows, q, k_cache, v_cache, block_tables,
+                                     context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                     num_blocks, block_size, max_blocks, scale, dtype, dtype, 1.0f,
+                                     1.0f, num_threads);
 }
 
 /* Number of threads an OpenMP region uses by default (1 without OpenMP). */

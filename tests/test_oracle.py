@@ -356,3 +356,93 @@ def test_decode_rejects_bad_tables():
     with pytest.raises(oracle.OracleError):
         oracle.paged_decode(q, kc, kc, torch.tensor([[0, 1]], dtype=torch.int32),
                             torch.tensor([5], dtype=torch.int32), 1, 1.0)
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) KV cache: codes, the scaled append, attention over scaled codes
+# --------------------------------------------------------------------------
+
+def test_e4m3_decode_every_code_matches_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    got = oracle.widen_e4m3(codes)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    assert ((got == ref) | (got.isnan() & ref.isnan())).all()
+    assert got[0x7E] == 448 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def test_e4m3_encode_rounds_like_torch_in_range():
+    gen = torch.Generator().manual_seed(3)
+    x = torch.cat([torch.randn(200000, generator=gen) * s for s in (1e-3, 1.0, 30.0, 200.0)])
+    # every midpoint between neighbouring finite codes (ties go to the even code)
+    v = oracle.widen_e4m3(torch.arange(0x7F, dtype=torch.uint8))
+    mids = ((v[1:] + v[:-1]) / 2).to(torch.float32)
+    x = torch.cat([x, mids, -mids])
+    keep = x.abs() < 464  # torch turns larger magnitudes into NaN, E4M3 here saturates
+    got = oracle.e4m3_encode(x[keep])
+    ref = x[keep].to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(got, ref)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    x = torch.tensor([448.0, 463.9, 464.0, 1e6, -1e6, float("inf"), float("-inf"), float("nan"), -0.0])
+    got = oracle.e4m3_encode(x).tolist()
+    assert got[:7] == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E, 0xFE]
+    assert got[7] & 0x7F == 0x7F and got[8] == 0x80
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_e4m3_append_stores_scaled_codes(dtype):
+    gen = torch.Generator().manual_seed(9)
+    T, Hkv, D, nb, bs = 7, 2, 64, 6, 8
+    key = (torch.randn(T, Hkv, D, generator=gen) * 3).to(dtype)
+    value = (torch.randn(T, Hkv, D, generator=gen) * 3).to(dtype)
+    kc = torch.full((nb, Hkv, bs, D), 0x55, dtype=torch.uint8)
+    vc = kc.clone()
+    slots = torch.tensor([3, 17, -1, 40, 0, 47, 9], dtype=torch.int64)
+    ks, vs = 0.0371, 2.5
+    oracle.reshape_and_cache_e4m3(key, value, kc, vc, slots, ks, vs)
+    inv_k = torch.tensor(oracle.inv_scale(ks), dtype=torch.float32)
+    inv_v = torch.tensor(oracle.inv_scale(vs), dtype=torch.float32)
+    for t, s in enumerate(slots.tolist()):
+        if s < 0:
+            continue
+        yk = key[t].to(torch.float32) * inv_k
+        yv = value[t].to(torch.float32) * inv_v
+        assert (yk.abs() < 464).all() and (yv.abs() < 464).all()
+        assert torch.equal(kc[s // bs, :, s % bs], yk.to(torch.float8_e4m3fn).view(torch.uint8))
+        assert torch.equal(vc[s // bs, :, s % bs], yv.to(torch.float8_e4m3fn).view(torch.uint8))
+    written = {(s // bs, s % bs) for s in slots.tolist() if s >= 0}
+    for b in range(nb):
+        for o in range(bs):
+            if (b, o) not in written:
+                assert (kc[b, :, o] == 0x55).all() and (vc[b, :, o] == 0x55).all()
+
+
+@pytest.mark.parametrize("qdtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 2, 128, 16), (32, 32, 128, 16), (28, 4, 256, 8)])
+def test_e4m3_decode_matches_dense_sdpa_on_scaled_codes(qdtype, Hq, Hkv, D, bs):
+    gen = torch.Generator().manual_seed(Hq + D + bs)
+    lens = [1, 9, bs, 3 * bs + 2, 50]
+    dk = [torch.randn(L, Hkv, D, generator=gen).to(torch.float8_e4m3fn) for L in lens]
+    dv = [torch.randn(L, Hkv, D, generator=gen).to(torch.float8_e4m3fn) for L in lens]
+    q = torch.randn(len(lens), Hq, D, generator=gen).to(qdtype)
+    ks, vs, scale = 0.731, 1.0 / 3.0, float(np.float32(1 / math.sqrt(D)))
+    nb = sum((L + bs - 1) // bs for L in lens) + 3
+    kp, vp, bt = paged_from_dense(dk, dv, bs, nb, gen, pad_blocks=1)
+    got = oracle.paged_decode(q, kp.view(torch.uint8), vp.view(torch.uint8), bt,
+                              torch.tensor(lens, dtype=torch.int32), Hkv, scale, k_scale=ks, v_scale=vs)
+    k64 = [k.to(torch.float64) * float(np.float32(ks)) for k in dk]
+    v64 = [v.to(torch.float64) * float(np.float32(vs)) for v in dv]
+    ref = _dense_sdpa(q, k64, v64, scale)
+    torch.testing.assert_close(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_one_token_returns_scaled_value_exactly():
+    v = torch.tensor([[[0.5, -3.0, 448.0, 2.0 ** -9]]]).to(torch.float8_e4m3fn)  # [1 token, 1 head, 4]
+    k = torch.ones(1, 1, 4).to(torch.float8_e4m3fn)
+    kp, vp, bt = paged_from_dense([k], [v], 4, 2, torch.Generator().manual_seed(0))
+    q = torch.ones(1, 2, 4, dtype=torch.float16)
+    got = oracle.paged_decode(q, kp.view(torch.uint8), vp.view(torch.uint8), bt, torch.tensor([1], dtype=torch.int32),
+                              1, 0.5, k_scale=3.0, v_scale=0.1)
+    vs = float(np.float32(0.1))
+    assert got[0, 0].tolist() == [0.5 * vs, -3.0 * vs, 448.0 * vs, 2.0 ** -9 * vs]

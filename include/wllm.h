@@ -41,7 +41,8 @@
  *     number s names block s / block_size, offset s % block_size.
  *   - Element types: q, out, key, value and both caches share one type:
  *     WLLM_F32, WLLM_F16 or WLLM_BF16.  Accumulation is fp32 throughout; fp32
- *     inputs never go through reduced-precision tensor-core math.
+ *     inputs never go through reduced-precision tensor-core math.  The *_fp8
+ *     calls below take caches of WLLM_FP8_E4M3 codes instead.
  */
 #ifndef WLLM_H_
 #define WLLM_H_
@@ -67,7 +68,9 @@ typedef enum {
   WLLM_F16 = 1,
   WLLM_BF16 = 2,
   WLLM_I32 = 3,
-  WLLM_I64 = 4
+  WLLM_I64 = 4,
+  WLLM_FP8_E4M3 = 5  /* one byte: OCP E4M3 "fn" (bias 7, no infinities,      */
+                     /* 0x7f/0xff NaN, largest finite +-448)                */
 } wllm_dtype;
 
 #define WLLM_MAX_DIMS 4
@@ -175,6 +178,65 @@ int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_te
                      const wllm_tensor* slot_mapping, const wllm_tensor* block_tables,
                      const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
                      wllm_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) KV cache.
+ *
+ * Passage: "wLLM" project page, "Features / Core engine" (the paged KV cache
+ * and its decode kernel; storing the cache in fewer bytes is the lever on a
+ * step that reads the whole cache).  The storage format is this library's
+ * reading: each cache element is the E4M3 code of the element divided by a
+ * per-tensor scale (one k_scale for every K element, one v_scale for every V
+ * element, binary32, positive and finite):
+ *
+ *   code = E4M3( fp32(x) * fp32(1 / scale) )
+ *
+ * the product rounded to binary32, then to the nearest E4M3 value (ties to
+ * even), magnitudes above 448 saturating to +-448 (NaN stays NaN).  Reading
+ * dequantises value(code) * scale.  Layout, slots, block tables, lengths and
+ * every other argument and check are those of the calls above.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * KV append into E4M3 caches.  key, value: [T][Hkv][D] F32/F16/BF16 (one
+ * type), last dimension contiguous, aligned to their element size; caches
+ * [N_b][Hkv][bs][D] WLLM_FP8_E4M3, dense, 4-byte aligned; D a multiple of 4.
+ * Stores the codes defined above; padding (negative) slots write nothing.
+ */
+int wllm_reshape_and_cache_fp8(const wllm_tensor* key, const wllm_tensor* value,
+                               const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                               const wllm_tensor* slot_mapping, float k_scale, float v_scale,
+                               wllm_stream stream);
+
+/*
+ * Paged decode attention over E4M3 caches:
+ *   out[b][h] = sum_j softmax_j(scale * q.(k_scale * K_j)) * (v_scale * V_j)
+ * with K_j, V_j the dequantised codes.  q and out F16 or BF16 (one type),
+ * query rows 16-byte aligned; D 128 or 256.  The codes are widened to f16
+ * exactly on the device; bf16 queries are rounded to f16 for the tensor-core
+ * products (|q| must stay within the f16 range); accumulation is fp32.  Runs
+ * the persistent kernel with split-KV merged inside the launch, like
+ * wllm_paged_attention_decode (same workspace rules, graph-capturable with a
+ * caller workspace); shared-prefix grouping is not used.
+ */
+int wllm_paged_attention_decode_fp8(const wllm_tensor* out, const wllm_tensor* q,
+                                    const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                                    const wllm_tensor* block_tables,
+                                    const wllm_tensor* context_lens, int num_kv_heads,
+                                    float scale, float k_scale, float v_scale, int block_size,
+                                    wllm_stream stream);
+
+/*
+ * One decode step over E4M3 caches: wllm_reshape_and_cache_fp8 then
+ * wllm_paged_attention_decode_fp8 with the same scales, fused into one
+ * cooperative launch as in wllm_decode_step.
+ */
+int wllm_decode_step_fp8(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key,
+                         const wllm_tensor* value, const wllm_tensor* k_cache,
+                         const wllm_tensor* v_cache, const wllm_tensor* slot_mapping,
+                         const wllm_tensor* block_tables, const wllm_tensor* context_lens,
+                         int num_kv_heads, float scale, float k_scale, float v_scale,
+                         int block_size, wllm_stream stream);
 
 /*
  * Paged decode attention that allocates no device memory.

@@ -18,10 +18,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libwllm.so")
 
 WLLM_OK, WLLM_ERR_INVALID_ARG, WLLM_ERR_UNSUPPORTED, WLLM_ERR_OUT_OF_RANGE, WLLM_ERR_CUDA = range(5)
-_DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3, torch.int64: 4}
+# E4M3 caches may be passed as torch.float8_e4m3fn or as raw uint8 codes
+_DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3, torch.int64: 4,
+          torch.float8_e4m3fn: 5, torch.uint8: 5}
 
 # every symbol include/wllm.h declares
 EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode", "wllm_decode_step",
+            "wllm_reshape_and_cache_fp8", "wllm_paged_attention_decode_fp8", "wllm_decode_step_fp8",
             "wllm_paged_attention_decode_noalloc",
             "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
             "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version",
@@ -69,6 +72,15 @@ def load_library():
         lib.wllm_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                          ctypes.c_void_p]
         lib.wllm_decode_step.restype = ctypes.c_int
+        f32 = ctypes.c_float
+        lib.wllm_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, f32, f32, ctypes.c_void_p]
+        lib.wllm_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.wllm_paged_attention_decode_fp8.argtypes = [P, P, P, P, P, P, ctypes.c_int, f32, f32, f32,
+                                                        ctypes.c_int, ctypes.c_void_p]
+        lib.wllm_paged_attention_decode_fp8.restype = ctypes.c_int
+        lib.wllm_decode_step_fp8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int, f32, f32, f32, ctypes.c_int,
+                                             ctypes.c_void_p]
+        lib.wllm_decode_step_fp8.restype = ctypes.c_int
         lib.wllm_paged_attention_decode_noalloc.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
                                                             ctypes.c_int, ctypes.c_void_p]
         lib.wllm_paged_attention_decode_noalloc.restype = ctypes.c_int
@@ -188,6 +200,42 @@ def decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables
                                       context_lens)]
         _check(lib.wllm_decode_step(*[ctypes.byref(a) for a in args], int(num_kv_heads), float(scale),
                                     int(block_size), _stream_handle(dev)))
+    return out
+
+
+def reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scale: float, v_scale: float) -> None:
+    """KV append into E4M3 caches (uint8 or float8_e4m3fn): stores E4M3(x * (1/scale))."""
+    dev = _require_cuda(key, value, k_cache, v_cache, slot_mapping)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (key, value, k_cache, v_cache, slot_mapping)]
+        _check(lib.wllm_reshape_and_cache_fp8(*[ctypes.byref(a) for a in args], float(k_scale), float(v_scale),
+                                              _stream_handle(dev)))
+
+
+def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads: int,
+                               scale: float, k_scale: float, v_scale: float, block_size: int) -> torch.Tensor:
+    """Paged decode attention over E4M3 caches (K = code * k_scale, V = code * v_scale); returns ``out``."""
+    dev = _require_cuda(out, q, k_cache, v_cache, block_tables, context_lens)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (out, q, k_cache, v_cache, block_tables, context_lens)]
+        _check(lib.wllm_paged_attention_decode_fp8(*[ctypes.byref(a) for a in args], int(num_kv_heads),
+                                                   float(scale), float(k_scale), float(v_scale), int(block_size),
+                                                   _stream_handle(dev)))
+    return out
+
+
+def decode_step_fp8(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens,
+                    num_kv_heads: int, scale: float, k_scale: float, v_scale: float, block_size: int) -> torch.Tensor:
+    """decode_step over E4M3 caches: the append quantises with the same scales the attention reads back."""
+    dev = _require_cuda(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (out, q, key, value, k_cache, v_cache, slot_mapping, block_tables,
+                                      context_lens)]
+        _check(lib.wllm_decode_step_fp8(*[ctypes.byref(a) for a in args], int(num_kv_heads), float(scale),
+                                        float(k_scale), float(v_scale), int(block_size), _stream_handle(dev)))
     return out
 
 

@@ -24,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwllm.so")
 
-SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "decode_f16.cu", "decode_f32.cu", "block_manager.cpp"]
+SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "decode_f16.cu", "decode_f32.cu", "decode_f8_f16.cu",
+           "decode_f8_bf16.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -31,10 +31,27 @@ int launch_persistent_f16(int, int, const CUtensorMap&, const CUtensorMap&, cons
                           const AppendParams*, bool, cudaStream_t);
 int occupancy_persistent_bf16(int, int, int);
 int occupancy_persistent_f16(int, int, int);
+int launch_persistent_f8_bf16(int, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, bool,
+                              const AppendParams*, bool, cudaStream_t);
+int launch_persistent_f8_f16(int, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, bool,
+                             const AppendParams*, bool, cudaStream_t);
+int occupancy_persistent_f8_bf16(int, int);
+int occupancy_persistent_f8_f16(int, int);
 
 int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
-                             const AppendParams* ap, bool fuse_combine, cudaStream_t stream) {
+                             const AppendParams* ap, bool fuse_combine, bool kv_fp8, cudaStream_t stream) {
+  if (kv_fp8) {
+    if (head_tile != 8) return cudaErrorInvalidValue;
+    switch (dtype) {
+      case WLLM_BF16:
+        return launch_persistent_f8_bf16(head_dim, kmap, vmap, p, grid, separate_combine, ap, fuse_combine, stream);
+      case WLLM_F16:
+        return launch_persistent_f8_f16(head_dim, kmap, vmap, p, grid, separate_combine, ap, fuse_combine, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   switch (dtype) {
     case WLLM_BF16:
       return launch_persistent_bf16(head_dim, head_tile, kmap, vmap, p, grid, separate_combine, ap, fuse_combine,
@@ -47,13 +64,17 @@ int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUten
   }
 }
 
-int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs) {
+int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs, bool kv_fp8) {
+  if (kv_fp8)
+    return dtype == WLLM_BF16 ? occupancy_persistent_f8_bf16(head_dim, num_seqs)
+                              : occupancy_persistent_f8_f16(head_dim, num_seqs);
   return dtype == WLLM_BF16 ? occupancy_persistent_bf16(head_dim, head_tile, num_seqs)
                             : occupancy_persistent_f16(head_dim, head_tile, num_seqs);
 }
 
-int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v) {
-  if (v == DecodeVariant::kFma || dtype == WLLM_F32) return 8;
+int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v, bool kv_fp8) {
+  // the fp8 kernel's unit merge fits one ring slot with 8 heads only
+  if (kv_fp8 || v == DecodeVariant::kFma || dtype == WLLM_F32) return 8;
   // two 8-head n-tiles when a group needs them and registers allow (D <= 128)
   return (group > 8 && head_dim <= 128) ? 16 : 8;
 }
@@ -174,6 +195,7 @@ int elt_size(int dtype) {
     case WLLM_BF16: return 2;
     case WLLM_I32: return 4;
     case WLLM_I64: return 8;
+    case WLLM_FP8_E4M3: return 1;
     default: return 0;
   }
 }
@@ -249,9 +271,10 @@ int make_pool_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blo
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(WLLM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   const int elt = elt_size(dtype);
-  CUtensorMapDataType dt = dtype == WLLM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                           : dtype == WLLM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMapDataType dt = dtype == WLLM_F32        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : dtype == WLLM_F16      ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                           : dtype == WLLM_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv * bs),
                         static_cast<cuuint64_t>(num_blocks)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elt), static_cast<cuuint64_t>(hkv * bs * d * elt)};
@@ -328,18 +351,25 @@ bool env_is(const char* name, const char* value) {
 
 // Variant, kernel, partition size and workspace layout of one launch over B
 // sequences.  `q_bulk_ok`: query rows are 16-byte aligned (bulk-copyable).
+// `kv_fp8`: E4M3 caches, which only the persistent kernel reads.
 DecodePlan make_plan(int dt, int64_t B, int64_t hq, int64_t hkv, int64_t d, int64_t mb, int64_t bs,
-                     bool q_bulk_ok, int num_sms) {
+                     bool q_bulk_ok, int num_sms, bool kv_fp8 = false) {
   DecodePlan pl;
-  pl.variant = (dt == WLLM_F32 || env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kFma : DecodeVariant::kMma;
-  pl.persistent = pl.variant == DecodeVariant::kMma && q_bulk_ok && !env_is("WLLM_DECODE_KERNEL", "grid");
+  if (kv_fp8) {
+    pl.variant = DecodeVariant::kMma;
+    pl.persistent = true;
+  } else {
+    pl.variant = (dt == WLLM_F32 || env_flag("WLLM_FORCE_FMA")) ? DecodeVariant::kFma : DecodeVariant::kMma;
+    pl.persistent = pl.variant == DecodeVariant::kMma && q_bulk_ok && !env_is("WLLM_DECODE_KERNEL", "grid");
+  }
   const int64_t group = hq / hkv;
-  pl.head_tile = decode_head_tile(dt, static_cast<int>(d), static_cast<int>(group), pl.variant);
+  pl.head_tile = decode_head_tile(dt, static_cast<int>(d), static_cast<int>(group), pl.variant, kv_fp8);
   pl.tiles = static_cast<int>((group + pl.head_tile - 1) / pl.head_tile);
   const int64_t tokens_max = std::max<int64_t>(1, mb * bs);
   const int64_t z = hkv * pl.tiles;
   if (pl.persistent) {
-    const int occ = decode_persistent_occupancy(dt, static_cast<int>(d), pl.head_tile, static_cast<int>(B));
+    const int occ =
+        decode_persistent_occupancy(dt, static_cast<int>(d), pl.head_tile, static_cast<int>(B), kv_fp8);
     const int64_t n_ctas = int64_t(num_sms > 0 ? num_sms : 148) * occ;
     pl.part_tokens = choose_partition_persistent(B, z, tokens_max, n_ctas);
     while ((tokens_max + pl.part_tokens - 1) / pl.part_tokens > kPersistentMaxParts) pl.part_tokens *= 2;
@@ -377,10 +407,14 @@ const char* wllm_version(void) { return "wllm-gb300 0.1.0 (sm_103a)"; }
 
 namespace {
 
+bool positive_finite(float x) { return x > 0.f && x < INFINITY; }
+
 // Check the append arguments and fill `ap` (all but the error word).  Leaves
-// ap.num_tokens == 0 when there is nothing to write.
+// ap.num_tokens == 0 when there is nothing to write.  `kv_fp8`: the caches
+// hold E4M3 codes of key / k_scale and value / v_scale.
 int prepare_append(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
-                   const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, AppendParams& ap) {
+                   const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, AppendParams& ap,
+                   bool kv_fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
   int rc;
   if ((rc = check_desc(key, "key", 3)) || (rc = check_desc(value, "value", 3)) ||
       (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
@@ -388,8 +422,15 @@ int prepare_append(const wllm_tensor* key, const wllm_tensor* value, const wllm_
     return rc;
   const int dt = key->dtype;
   if (!is_float(dt)) return fail(WLLM_ERR_INVALID_ARG, "key: dtype must be F32, F16 or BF16");
-  if (value->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
+  if (kv_fp8) {
+    if (value->dtype != dt) return fail(WLLM_ERR_INVALID_ARG, "key and value must share one dtype");
+    if (k_cache->dtype != WLLM_FP8_E4M3 || v_cache->dtype != WLLM_FP8_E4M3)
+      return fail(WLLM_ERR_INVALID_ARG, "caches must be FP8_E4M3");
+    if (!positive_finite(k_scale) || !positive_finite(v_scale))
+      return fail(WLLM_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  } else if (value->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt) {
     return fail(WLLM_ERR_INVALID_ARG, "key, value and caches must share one dtype");
+  }
   if (slot_mapping->dtype != WLLM_I64 && slot_mapping->dtype != WLLM_I32)
     return fail(WLLM_ERR_INVALID_ARG, "slot_mapping: dtype must be I64 or I32");
   if (!same_shape(key, value)) return fail(WLLM_ERR_INVALID_ARG, "key and value shapes differ");
@@ -406,6 +447,8 @@ int prepare_append(const wllm_tensor* key, const wllm_tensor* value, const wllm_
   if (d > 1 && (key->stride[2] != 1 || value->stride[2] != 1))
     return fail(WLLM_ERR_INVALID_ARG, "key/value last dimension must be contiguous");
   if (!is_pow2(bs)) return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld is not a power of two", (long long)bs);
+  if (kv_fp8 && d % 4 != 0)
+    return fail(WLLM_ERR_UNSUPPORTED, "an fp8 cache needs head_dim a multiple of 4, got %lld", (long long)d);
   if (T > INT32_MAX || hkv > INT32_MAX || d * elt_size(dt) > INT32_MAX)
     return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
   ap = AppendParams{};
@@ -419,18 +462,28 @@ int prepare_append(const wllm_tensor* key, const wllm_tensor* value, const wllm_
   ap.slots_are_i64 = slot_mapping->dtype == WLLM_I64;
   ap.num_tokens = static_cast<int>(T);
   ap.num_kv_heads = static_cast<int>(hkv);
-  ap.row_bytes = static_cast<int>(d * elt);
+  ap.row_bytes = static_cast<int>(kv_fp8 ? d : d * elt);
   ap.key_st = key->stride[0] * elt;
   ap.key_sh = key->stride[1] * elt;
   ap.val_st = value->stride[0] * elt;
   ap.val_sh = value->stride[1] * elt;
   ap.log2_bs = ilog2(bs);
   ap.num_slots = nb * bs;
-  ap.vec16 = (ap.row_bytes % 16 == 0) && aligned(ap.key, 16) && aligned(ap.value, 16) && aligned(ap.k_cache, 16) &&
+  ap.vec16 = !kv_fp8 && (ap.row_bytes % 16 == 0) && aligned(ap.key, 16) && aligned(ap.value, 16) && aligned(ap.k_cache, 16) &&
              aligned(ap.v_cache, 16) && ap.key_st % 16 == 0 && ap.key_sh % 16 == 0 && ap.val_st % 16 == 0 &&
              ap.val_sh % 16 == 0;
-  if (!ap.vec16 && !(aligned(ap.key, 2) && aligned(ap.value, 2)))
+  if (kv_fp8) {
+    if (!(aligned(ap.key, elt) && aligned(ap.value, elt)))
+      return fail(WLLM_ERR_INVALID_ARG, "key/value must be aligned to their element size");
+    if (!(aligned(ap.k_cache, 4) && aligned(ap.v_cache, 4)))
+      return fail(WLLM_ERR_INVALID_ARG, "fp8 caches must be 4-byte aligned");
+    ap.kv_fp8 = 1;
+    ap.src_dtype = dt;
+    ap.k_inv = 1.f / k_scale;
+    ap.v_inv = 1.f / v_scale;
+  } else if (!ap.vec16 && !(aligned(ap.key, 2) && aligned(ap.value, 2))) {
     return fail(WLLM_ERR_INVALID_ARG, "key/value must be at least 2-byte aligned");
+  }
   return WLLM_OK;
 }
 
@@ -446,11 +499,13 @@ int check_append_slots(DeviceState* s, const AppendParams& ap, cudaStream_t st) 
 
 extern "C" {
 
-int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
-                           const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, wllm_stream stream) {
-  AppendParams ap{};
-  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap);
-  if (rc || ap.num_tokens == 0) return rc;
+}  // extern "C"
+
+namespace {
+
+// The append after its argument checks.
+int run_append(AppendParams& ap, wllm_stream stream) {
+  int rc;
   DeviceState* s = nullptr;
   if ((rc = device_state(&s))) return rc;
   ap.err = s->err;
@@ -461,6 +516,27 @@ int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, con
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   if (check) return collect_device_errors(s, st, "reshape_and_cache");
   return WLLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
+                           const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, wllm_stream stream) {
+  AppendParams ap{};
+  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap);
+  if (rc || ap.num_tokens == 0) return rc;
+  return run_append(ap, stream);
+}
+
+int wllm_reshape_and_cache_fp8(const wllm_tensor* key, const wllm_tensor* value, const wllm_tensor* k_cache,
+                               const wllm_tensor* v_cache, const wllm_tensor* slot_mapping, float k_scale,
+                               float v_scale, wllm_stream stream) {
+  AppendParams ap{};
+  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap, true, k_scale, v_scale);
+  if (rc || ap.num_tokens == 0) return rc;
+  return run_append(ap, stream);
 }
 
 size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -479,6 +555,12 @@ size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int n
                                       max_blocks_per_seq, block_size, bulk, sms);
       need = std::max(need, pl.counter_bytes + pl.ml_bytes + pl.o_bytes);
     }
+  }
+  if (head_dim == 128 || head_dim == 256) {  // decode over an fp8 cache
+    const int64_t B = std::min<int64_t>(num_seqs, kPersistentMaxSeqs);
+    const DecodePlan pl = make_plan(WLLM_BF16, B, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                    block_size, true, sms, true);
+    need = std::max(need, pl.counter_bytes + pl.ml_bytes + pl.o_bytes);
   }
   return need;
 }
@@ -576,24 +658,39 @@ int bind_workspace(DeviceState* s, const DecodePlan& pl, cudaStream_t st, Decode
 namespace {
 
 struct DecodeArgs {
-  int dt = 0, elt = 0;
+  int dt = 0, elt = 0;  // query / output type and its size
+  int kv_dt = 0;        // cache element type (dt, or WLLM_FP8_E4M3)
   int64_t B = 0, hq = 0, d = 0, nb = 0, hkv = 0, bs = 0, mb = 0;
   bool q_bulk_ok = false;
+  bool kv_fp8 = false;
+  float k_scale = 1.f, v_scale = 1.f;
 };
 
 // Check the decode arguments; a.B == 0 (or no heads) means nothing to do.
+// `kv_fp8`: E4M3 caches holding K / k_scale and V / v_scale.
 int prepare_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
                    const wllm_tensor* v_cache, const wllm_tensor* block_tables, const wllm_tensor* context_lens,
-                   int num_kv_heads, float scale, int block_size, DecodeArgs& a) {
+                   int num_kv_heads, float scale, int block_size, DecodeArgs& a, bool kv_fp8 = false,
+                   float k_scale = 1.f, float v_scale = 1.f) {
   int rc;
   if ((rc = check_desc(out, "out", 3)) || (rc = check_desc(q, "q", 3)) ||
       (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
       (rc = check_desc(block_tables, "block_tables", 2)) || (rc = check_desc(context_lens, "context_lens", 1)))
     return rc;
   const int dt = q->dtype;
-  if (!is_float(dt)) return fail(WLLM_ERR_INVALID_ARG, "q: dtype must be F32, F16 or BF16");
-  if (out->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
-    return fail(WLLM_ERR_INVALID_ARG, "q, out and caches must share one dtype");
+  if (kv_fp8) {
+    if (dt != WLLM_F16 && dt != WLLM_BF16)
+      return fail(WLLM_ERR_INVALID_ARG, "q: dtype must be F16 or BF16 with an fp8 cache");
+    if (out->dtype != dt) return fail(WLLM_ERR_INVALID_ARG, "out must have the dtype of q");
+    if (k_cache->dtype != WLLM_FP8_E4M3 || v_cache->dtype != WLLM_FP8_E4M3)
+      return fail(WLLM_ERR_INVALID_ARG, "caches must be FP8_E4M3");
+    if (!positive_finite(k_scale) || !positive_finite(v_scale))
+      return fail(WLLM_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
+  } else {
+    if (!is_float(dt)) return fail(WLLM_ERR_INVALID_ARG, "q: dtype must be F32, F16 or BF16");
+    if (out->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
+      return fail(WLLM_ERR_INVALID_ARG, "q, out and caches must share one dtype");
+  }
   if (block_tables->dtype != WLLM_I32) return fail(WLLM_ERR_INVALID_ARG, "block_tables: dtype must be I32");
   if (context_lens->dtype != WLLM_I32) return fail(WLLM_ERR_INVALID_ARG, "context_lens: dtype must be I32");
   if (!same_shape(out, q)) return fail(WLLM_ERR_INVALID_ARG, "out and q shapes differ");
@@ -623,7 +720,12 @@ int prepare_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tens
     return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
   if (B > INT32_MAX || hq > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
     return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  if (kv_fp8 && d == 64) return fail(WLLM_ERR_UNSUPPORTED, "an fp8 cache needs head_dim 128 or 256");
   a = DecodeArgs{};
+  a.kv_dt = kv_fp8 ? WLLM_FP8_E4M3 : dt;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.dt = dt;
   a.B = B;
   a.hq = hq;
@@ -641,6 +743,8 @@ int prepare_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tens
   a.bs = bs;
   a.mb = mb;
   a.q_bulk_ok = aligned(q->data, 16) && (q->stride[0] * elt) % 16 == 0 && (q->stride[1] * elt) % 16 == 0;
+  if (kv_fp8 && !a.q_bulk_ok)
+    return fail(WLLM_ERR_UNSUPPORTED, "decode over an fp8 cache needs 16-byte aligned query rows");
   return WLLM_OK;
 }
 
@@ -652,8 +756,8 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
                float scale, DeviceState* s, cudaStream_t st, const AppendParams* fuse_ap) {
   int rc;
   CUtensorMap kmap, vmap;
-  if ((rc = make_pool_map(&kmap, k_cache->data, a.dt, a.nb, a.hkv, a.bs, a.d, "k_cache"))) return rc;
-  if ((rc = make_pool_map(&vmap, v_cache->data, a.dt, a.nb, a.hkv, a.bs, a.d, "v_cache"))) return rc;
+  if ((rc = make_pool_map(&kmap, k_cache->data, a.kv_dt, a.nb, a.hkv, a.bs, a.d, "k_cache"))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, a.kv_dt, a.nb, a.hkv, a.bs, a.d, "v_cache"))) return rc;
   const bool check = env_flag("WLLM_CHECK");
   if (check) {
     cudaError_t e = static_cast<cudaError_t>(launch_check_decode(
@@ -667,11 +771,11 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
   // with the decode, unless asked otherwise
   const bool separate_kernel = env_flag("WLLM_SEPARATE_COMBINE");
   const DecodePlan first = make_plan(a.dt, std::min<int64_t>(a.B, kPersistentMaxSeqs), a.hq, a.hkv, a.d, a.mb,
-                                     a.bs, a.q_bulk_ok, s->num_sms);
+                                     a.bs, a.q_bulk_ok, s->num_sms, a.kv_fp8);
   const int64_t slice = first.persistent ? kPersistentMaxSeqs : a.B;
   for (int64_t b0 = 0; b0 < a.B; b0 += slice) {
     const int64_t nbat = std::min<int64_t>(slice, a.B - b0);
-    const DecodePlan pl = make_plan(a.dt, nbat, a.hq, a.hkv, a.d, a.mb, a.bs, a.q_bulk_ok, s->num_sms);
+    const DecodePlan pl = make_plan(a.dt, nbat, a.hq, a.hkv, a.d, a.mb, a.bs, a.q_bulk_ok, s->num_sms, a.kv_fp8);
     DecodeParams p{};
     p.out = static_cast<uint8_t*>(out->data) + b0 * out->stride[0] * a.elt;
     p.q = static_cast<const uint8_t*>(q->data) + b0 * q->stride[0] * a.elt;
@@ -694,7 +798,9 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
     p.num_blocks = static_cast<int>(a.nb);
     p.part_tokens = pl.part_tokens;
     p.max_parts = pl.max_parts;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    // an fp8 cache holds K / k_scale: the scale returns in the softmax scale
+    p.scale_log2 = (a.kv_fp8 ? scale * a.k_scale : scale) * 1.4426950408889634f;
+    p.v_scale = a.v_scale;
     p.err = s->err;
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
     p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 1) != 0;
@@ -705,7 +811,8 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
       const AppendParams* ap = b0 == 0 ? fuse_ap : nullptr;
       const bool fuse_combine = pl.max_parts > 1 && !separate_kernel;
       e = static_cast<cudaError_t>(launch_decode_persistent(a.dt, static_cast<int>(a.d), pl.head_tile, kmap, vmap,
-                                                            p, pl.grid, pl.separate_combine, ap, fuse_combine, st));
+                                                            p, pl.grid, pl.separate_combine, ap, fuse_combine,
+                                                            a.kv_fp8, st));
     } else {
       if (b0 == 0 && fuse_ap != nullptr) {  // no fused form for this kernel: append first
         e = static_cast<cudaError_t>(launch_append(*fuse_ap, st));
@@ -723,12 +830,17 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
 
 extern "C" {
 
-int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
-                                const wllm_tensor* v_cache, const wllm_tensor* block_tables,
-                                const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
-                                wllm_stream stream) {
+}  // extern "C"
+
+namespace {
+
+int decode_call(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                const wllm_tensor* v_cache, const wllm_tensor* block_tables, const wllm_tensor* context_lens,
+                int num_kv_heads, float scale, int block_size, wllm_stream stream, bool kv_fp8, float k_scale,
+                float v_scale) {
   DecodeArgs a;
-  int rc = prepare_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, a);
+  int rc = prepare_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, a,
+                          kv_fp8, k_scale, v_scale);
   if (rc || a.B == 0 || a.hq == 0) return rc;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState* s = nullptr;
@@ -737,15 +849,16 @@ int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, co
                     reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
-int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key, const wllm_tensor* value,
-                     const wllm_tensor* k_cache, const wllm_tensor* v_cache, const wllm_tensor* slot_mapping,
-                     const wllm_tensor* block_tables, const wllm_tensor* context_lens, int num_kv_heads, float scale,
-                     int block_size, wllm_stream stream) {
+int step_call(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key, const wllm_tensor* value,
+              const wllm_tensor* k_cache, const wllm_tensor* v_cache, const wllm_tensor* slot_mapping,
+              const wllm_tensor* block_tables, const wllm_tensor* context_lens, int num_kv_heads, float scale,
+              int block_size, wllm_stream stream, bool kv_fp8, float k_scale, float v_scale) {
   AppendParams ap{};
-  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap);
+  int rc = prepare_append(key, value, k_cache, v_cache, slot_mapping, ap, kv_fp8, k_scale, v_scale);
   if (rc) return rc;
   DecodeArgs a;
-  if ((rc = prepare_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, a)))
+  if ((rc = prepare_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, a,
+                           kv_fp8, k_scale, v_scale)))
     return rc;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState* s = nullptr;
@@ -761,6 +874,43 @@ int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_te
   }
   return run_decode(a, out, q, k_cache, v_cache, block_tables, context_lens, scale, s, st,
                     have_append ? &ap : nullptr);
+}
+
+}  // namespace
+
+extern "C" {
+
+int wllm_paged_attention_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
+                                wllm_stream stream) {
+  return decode_call(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, stream,
+                     false, 1.f, 1.f);
+}
+
+int wllm_paged_attention_decode_fp8(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                    const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                    const wllm_tensor* context_lens, int num_kv_heads, float scale, float k_scale,
+                                    float v_scale, int block_size, wllm_stream stream) {
+  return decode_call(out, q, k_cache, v_cache, block_tables, context_lens, num_kv_heads, scale, block_size, stream,
+                     true, k_scale, v_scale);
+}
+
+int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key, const wllm_tensor* value,
+                     const wllm_tensor* k_cache, const wllm_tensor* v_cache, const wllm_tensor* slot_mapping,
+                     const wllm_tensor* block_tables, const wllm_tensor* context_lens, int num_kv_heads, float scale,
+                     int block_size, wllm_stream stream) {
+  return step_call(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens, num_kv_heads,
+                   scale, block_size, stream, false, 1.f, 1.f);
+}
+
+int wllm_decode_step_fp8(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* key,
+                         const wllm_tensor* value, const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                         const wllm_tensor* slot_mapping, const wllm_tensor* block_tables,
+                         const wllm_tensor* context_lens, int num_kv_heads, float scale, float k_scale,
+                         float v_scale, int block_size, wllm_stream stream) {
+  return step_call(out, q, key, value, k_cache, v_cache, slot_mapping, block_tables, context_lens, num_kv_heads,
+                   scale, block_size, stream, true, k_scale, v_scale);
 }
 
 // ---------------------------------------------------------------------------
@@ -915,6 +1065,7 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
     p.part_tokens = pl.part_tokens;
     p.max_parts = pl.max_parts;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.v_scale = 1.f;
     p.err = reinterpret_cast<int*>(scratch);
     p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
     p.prefix_groups = env_int("WLLM_PREFIX_GROUPS", 1) != 0;
@@ -922,7 +1073,7 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
     p.ws_ml = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes) : nullptr;
     p.ws_o = pl.ml_bytes ? reinterpret_cast<float*>(scratch + kNoAllocControlBytes + pl.ml_bytes) : nullptr;
     e = static_cast<cudaError_t>(launch_decode_persistent(dt, static_cast<int>(d), pl.head_tile, kmap, vmap, p,
-                                                          pl.grid, pl.separate_combine, nullptr, false, st));
+                                                          pl.grid, pl.separate_combine, nullptr, false, false, st));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return WLLM_OK;

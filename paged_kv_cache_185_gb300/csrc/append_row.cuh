@@ -1,7 +1,8 @@
 // append_row.cuh -- one (token, kv head) row of the KV append, done by one
 // warp: the token's K row and V row (head_dim elements each) are copied bit
-// for bit into slot slot_mapping[t] of the caches.  Shared by the append
-// kernel and the fused decode step.
+// for bit into slot slot_mapping[t] of the caches, or, for an fp8 cache,
+// stored as scaled E4M3 codes.  Shared by the append kernel and the fused
+// decode step.
 #pragma once
 
 #include "common.cuh"
@@ -27,6 +28,30 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int64_t row, i
   const uint8_t* vs = p.value + t * p.val_st + h * p.val_sh;
   uint8_t* kd = p.k_cache + dst;
   uint8_t* vd = p.v_cache + dst;
+  if (p.kv_fp8) {
+    // E4M3 codes of x * (1/scale): the product rounded to binary32, then to
+    // the nearest code (ties to even), saturating at +-448.  Lane u of the row
+    // handles four consecutive elements (head_dim is a multiple of 4).
+    const int n4 = p.row_bytes >> 2;
+    for (int u = lane; u < 2 * n4; u += 32) {
+      const bool is_k = u < n4;
+      const int j = is_k ? u : u - n4;
+      const uint8_t* src = is_k ? ks : vs;
+      const float inv = is_k ? p.k_inv : p.v_inv;
+      float x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = 4 * j + i;
+        x[i] = p.src_dtype == 0   ? reinterpret_cast<const float*>(src)[e]
+               : p.src_dtype == 1 ? __half2float(reinterpret_cast<const __half*>(src)[e])
+                                  : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(src)[e]);
+        x[i] = __fmul_rn(x[i], inv);
+      }
+      const uint32_t lo = f32x2_to_e4m3x2(x[1], x[0]), hi = f32x2_to_e4m3x2(x[3], x[2]);
+      reinterpret_cast<uint32_t*>(is_k ? kd : vd)[j] = lo | (hi << 16);
+    }
+    return;
+  }
   if (p.vec16) {
     const int n = p.row_bytes >> 4;  // 16-byte units per row
     for (int u = lane; u < 2 * n; u += 32) {

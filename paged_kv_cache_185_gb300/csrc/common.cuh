@@ -182,6 +182,21 @@ struct Mma<__half> {
 // ---------------------------------------------------------------------------
 // element conversion
 // ---------------------------------------------------------------------------
+// Two E4M3 codes (low byte -> low half) widened to f16x2; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+  uint32_t y;
+  const uint16_t x = static_cast<uint16_t>(pair16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));
+  return y;
+}
+
+// E4M3 codes of (hi, lo): round to nearest even, saturating at +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float hi, float lo) {
+  uint16_t y;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(y) : "f"(hi), "f"(lo));
+  return y;
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

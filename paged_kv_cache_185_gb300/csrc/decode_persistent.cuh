@@ -39,6 +39,7 @@
 
 #include "append_row.cuh"
 #include "decode_kernel.cuh"
+#include "mma_e4m3.cuh"
 
 namespace wllm {
 
@@ -135,12 +136,15 @@ struct DoneInfo {
 };
 constexpr int kDoneSlots = 4;
 
-template <typename T, int D, int NT>
+// F8: the KV cache holds E4M3 codes (one byte per element); T is the query
+// and output type.
+template <typename T, int D, int NT, bool F8 = false>
 struct PShape {
   static constexpr int kConsumers = 4;
   static constexpr int kThreads = (kConsumers + 2) * 32;  // consumers, producer, scheduler
   static constexpr int kHeadTile = 8 * NT;
-  static constexpr int kKV = Geom<T, D>::kTileBytes;  // one 16-row K (or V) sub-tile
+  using KT = typename std::conditional<F8, uint8_t, T>::type;  // cache element
+  static constexpr int kKV = Geom<KT, D>::kTileBytes;  // one 16-row K (or V) sub-tile
   static constexpr int kQBytes = kHeadTile * D * static_cast<int>(sizeof(T));
   static constexpr int kStageBytes = ((2 * kSub * kKV + kQBytes) + 1023) / 1024 * 1024;
   // the unit merge writes each consumer's (m, l, O) into the ring slot of
@@ -505,17 +509,18 @@ __device__ __forceinline__ void finish_members(MmaState<T, D, NT>& st, const Dec
   }
 }
 
-template <typename T, int D, int NT>
-__global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShape<T, D, NT>::kMaxRegs))
+template <typename T, int D, int NT, bool F8>
+__global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((PShape<T, D, NT, F8>::kMaxRegs))
     paged_decode_persistent(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                             const DecodeParams p, const AppendParams ap, const int flags) {
-  using G = Geom<T, D>;
-  using PS = PShape<T, D, NT>;
+  using PS = PShape<T, D, NT, F8>;
+  using G = Geom<typename PS::KT, D>;
+  using MT = typename std::conditional<F8, __half, T>::type;  // tensor-core operand type
   constexpr int S = PS::kStages;
   constexpr int W = PS::kConsumers;
   constexpr int HT = PS::kHeadTile;
   constexpr int Q = kQueue;
-  constexpr bool kGroupOK = NT == 1 && D <= 128;
+  constexpr bool kGroupOK = NT == 1 && D <= 128 && !F8;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1108,7 +1113,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     if (threadIdx.x == 0) mbar_arrive(smem_u32(pbar));
   }
   if ((flags & kFuseAppend) && !cta_grid_sync()) failed = true;
-  MmaState<T, D, NT> st;
+  MmaState<MT, D, NT> st;
   const int cw = warp;
   const uint32_t sync_bar = smem_u32(cbar);
   int sync_phase = 0;
@@ -1188,10 +1193,18 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
       }
     }
     if (!(mt_.flags & kEmptySeq)) {
-      if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, ring + s * PS::kStageBytes + 2 * kSub * PS::kKV, mt_.nh, lane);
-      if (cw < mt_.nsub)
-        mma_chunk<T, D, NT>(st, stage + cw * PS::kKV, stage + (kSub + cw) * PS::kKV, mt_.t0 + cw * kChunk,
-                            mt_.tok_end, p.scale_log2, lane);
+      const uint8_t* qtile = ring + s * PS::kStageBytes + 2 * kSub * PS::kKV;
+      if constexpr (F8) {
+        if (mt_.flags & kFirst) load_q_smem_e4m3<T, D, NT>(st, qtile, mt_.nh, lane);
+        if (cw < mt_.nsub)
+          mma_chunk_e4m3<D, NT>(st, stage + cw * PS::kKV, stage + (kSub + cw) * PS::kKV, mt_.t0 + cw * kChunk,
+                                mt_.tok_end, p.scale_log2, lane);
+      } else {
+        if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, qtile, mt_.nh, lane);
+        if (cw < mt_.nsub)
+          mma_chunk<T, D, NT>(st, stage + cw * PS::kKV, stage + (kSub + cw) * PS::kKV, mt_.t0 + cw * kChunk,
+                              mt_.tok_end, p.scale_log2, lane);
+      }
     }
     __syncwarp();
     // the slot of a unit's last stage is kept for the merge and released after it
@@ -1218,7 +1231,10 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
     float* red_o = reinterpret_cast<float*>(ring + s * PS::kStageBytes);  // [W][HT][D]
     float* red_m = red_o + W * HT * D;                                      // [W][HT]
     float* red_l = red_m + W * HT;                                          // [W][HT]
-    mma_store<T, D, NT>(st, red_o + cw * HT * D, red_m + cw * HT, red_l + cw * HT, lane);
+    if constexpr (F8)
+      mma_store_e4m3<D, NT>(st, red_o + cw * HT * D, red_m + cw * HT, red_l + cw * HT, lane);
+    else
+      mma_store<T, D, NT>(st, red_o + cw * HT * D, red_m + cw * HT, red_l + cw * HT, lane);
     if (!consumer_sync(sync_bar, sync_phase, p.wait_limit_ns, lane)) {
       if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
       failed = true;
@@ -1239,8 +1255,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
         fw[w] = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
         den += fw[w] * red_l[w * HT + hh];
       }
+      // an fp8 cache holds V / v_scale: the scale comes back here (the
+      // partials carry it into the split merge)
+      const float vsc = F8 ? p.v_scale : 1.f;
       if (!split) {
-        const float inv = 1.f / den;
+        const float inv = vsc / den;
         T* orow = out + b * p.o_sb + static_cast<int64_t>(h0 + hh) * p.o_sh;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
@@ -1259,7 +1278,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT>::kThreads) __maxnreg__((PShap
           float num = 0.f;
 #pragma unroll
           for (int w = 0; w < W; ++w) num += fw[w] * red_o[(w * HT + hh) * D + d];
-          wo[d] = num;
+          wo[d] = F8 ? num * vsc : num;
         }
         if (lane == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, den);
       }
@@ -1386,9 +1405,9 @@ __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
   combine_rows<T, D, 1>(p, rows, threadIdx.x & 31);
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool F8>
 int persistent_smem(int num_seqs) {
-  return PShape<T, D, NT>::kFixedSmem + ((num_seqs + 1 + 3) & ~3) * 4 + kOrderKeys * 4 + (num_seqs * 3 + 15) / 16 * 16;
+  return PShape<T, D, NT, F8>::kFixedSmem + ((num_seqs + 1 + 3) & ~3) * 4 + kOrderKeys * 4 + (num_seqs * 3 + 15) / 16 * 16;
 }
 
 // Launch the persistent decode.  `ap` non-null fuses the KV append in front of
@@ -1398,13 +1417,13 @@ int persistent_smem(int num_seqs) {
 // waits need every CTA resident; the grid never exceeds SMs x occupancy).
 // Otherwise split partitions are merged by the separate combine kernel when
 // `separate_combine` is set.
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool F8 = false>
 int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p, int grid,
                            bool separate_combine, const AppendParams* ap, bool fuse_combine,
                            cudaStream_t stream) {
-  using PS = PShape<T, D, NT>;
-  auto kernel = paged_decode_persistent<T, D, NT>;
-  const int smem = persistent_smem<T, D, NT>(p.num_seqs);
+  using PS = PShape<T, D, NT, F8>;
+  auto kernel = paged_decode_persistent<T, D, NT, F8>;
+  const int smem = persistent_smem<T, D, NT, F8>(p.num_seqs);
   static int configured_for[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1441,15 +1460,15 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
   return cudaGetLastError();
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool F8 = false>
 int persistent_occupancy(int num_seqs) {
   int blocks = 0;
-  const int smem = persistent_smem<T, D, NT>(num_seqs);
-  if (cudaFuncSetAttribute(paged_decode_persistent<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int smem = persistent_smem<T, D, NT, F8>(num_seqs);
+  if (cudaFuncSetAttribute(paged_decode_persistent<T, D, NT, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024) != cudaSuccess)
     return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_persistent<T, D, NT>,
-                                                    PShape<T, D, NT>::kThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_persistent<T, D, NT, F8>,
+                                                    PShape<T, D, NT, F8>::kThreads, smem) != cudaSuccess)
     return 1;
   return blocks < 1 ? 1 : blocks;
 }

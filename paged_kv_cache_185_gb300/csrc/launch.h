@@ -21,7 +21,8 @@ struct DecodeParams {
   int head_tile, num_head_tiles;  // query heads per CTA, tiles per kv head
   int max_blocks, block_size, log2_bs, num_blocks;
   int part_tokens, max_parts;     // split-KV partition size / count
-  float scale_log2;               // scale * log2(e)
+  float scale_log2;               // scale * log2(e) (times k_scale for an fp8 cache)
+  float v_scale;                  // fp8 cache: factor of every output (1 otherwise)
   float* ws_o;                    // [B*Hq][max_parts][D] unnormalised partial sums
   float* ws_ml;                   // [B*Hq][max_parts][2] running max (log2 units), sum
   int* ws_count;                  // counters, zero between calls: grid kernel [B*Hkv*tiles] arrivals;
@@ -39,12 +40,15 @@ struct AppendParams {
   const void* slots;
   int slots_are_i64;
   int num_tokens, num_kv_heads;
-  int row_bytes;                  // head_dim * element size
+  int row_bytes;                  // bytes of one cache row: head_dim * cache element size
   int64_t key_st, key_sh;         // strides in bytes
   int64_t val_st, val_sh;
   int log2_bs;
   int64_t num_slots;              // num_blocks * block_size
   int vec16;                      // rows and strides allow 16-byte copies
+  int kv_fp8;                     // caches hold E4M3 codes of key * k_inv and value * v_inv
+  int src_dtype;                  // fp8: key/value element type, a wllm_dtype code (0 f32, 1 f16, 2 bf16)
+  float k_inv, v_inv;             // fp8: binary32 reciprocals of the scales
   int* err;
 };
 
@@ -52,7 +56,7 @@ struct AppendParams {
 enum class DecodeVariant { kMma, kFma };
 
 // Head tile (query heads of one KV head handled by one CTA) for a variant.
-int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v);
+int decode_head_tile(int dtype, int head_dim, int group, DecodeVariant v, bool kv_fp8);
 
 // Launch the decode kernel; returns a cudaError_t value.
 int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& kmap,
@@ -64,10 +68,12 @@ int launch_decode(int dtype, int head_dim, DecodeVariant v, const CUtensorMap& k
 // fuses the KV append in front; `fuse_combine` merges the partitions inside
 // the launch, as they complete (p.ws_count must then hold the zeroed
 // counters).  Either makes it a cooperative launch.
+// `kv_fp8`: the caches hold E4M3 codes (head_dim 128 or 256, head tile 8);
+// dtype is then the query / output type.
 int launch_decode_persistent(int dtype, int head_dim, int head_tile, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, int grid, bool separate_combine,
-                             const AppendParams* ap, bool fuse_combine, cudaStream_t stream);
-int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs);
+                             const AppendParams* ap, bool fuse_combine, bool kv_fp8, cudaStream_t stream);
+int decode_persistent_occupancy(int dtype, int head_dim, int head_tile, int num_seqs, bool kv_fp8);
 constexpr int kPersistentConsumers = 4;
 constexpr int kPersistentMaxSeqs = 1024;      // sequences per launch (the host splits larger batches)
 constexpr int kPersistentMaxParts = 256;      // partitions per sequence (the host widens partitions to fit)

@@ -35,7 +35,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-__all__ = ["DecodeCase", "make_case", "custom_case", "CASE_NAMES", "normal"]
+__all__ = ["DecodeCase", "make_case", "custom_case", "CASE_NAMES", "normal", "e4m3_codes"]
 
 
 def normal(seed: int, n: int) -> np.ndarray:
@@ -341,3 +341,20 @@ def make_case(name: str, replica: int = 0) -> DecodeCase:
     c4 (long-context, 32K-128K tokens, ~120 GB pool).  ``replica`` > 0 draws an
     independent batch of the same recipe (another seed)."""
     return _BUILDERS[name](replica)
+
+
+def e4m3_codes(x: torch.Tensor, amp: float = 1.0) -> torch.Tensor:
+    """Input codes for an fp8 (E4M3) cache: PyTorch's float8_e4m3fn cast of
+    float32(x) * amp, returned as uint8 (NaN slots stay NaN codes).  This draws
+    inputs only; the library's own append rule (which saturates) is not used
+    here, so finite values must stay below 448 in magnitude."""
+    flat = x.reshape(-1)
+    out = torch.empty(flat.shape, dtype=torch.uint8)
+    step = 1 << 26
+    for i in range(0, flat.numel(), step):
+        y = flat[i:i + step].to(torch.float32) * amp
+        fin = y[torch.isfinite(y)]
+        if fin.numel() and fin.abs().max().item() >= 448:
+            raise ValueError("values out of the E4M3 range: lower amp")
+        out[i:i + step] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out.reshape(x.shape)

@@ -116,3 +116,54 @@ def test_binding_refuses_host_tensors():
         binding.paged_attention_decode(torch.empty_like(q), q, kc, kc,
                                        torch.zeros(1, 1, dtype=torch.int32),
                                        torch.ones(1, dtype=torch.int32), 1, 0.1, 16)
+
+
+def decode_fp8(lib, out, q, kc, vc, bt, cl, hkv=2, scale=0.125, ks=0.5, vs=0.5, bs=16):
+    r = lambda x: None if x is None else ctypes.byref(x)  # noqa: E731
+    return lib.wllm_paged_attention_decode_fp8(r(out), r(q), r(kc), r(vc), r(bt), r(cl), hkv, scale, ks, vs, bs,
+                                               None)
+
+
+def good_fp8(B=2, Hq=4, Hkv=2, D=128, bs=16, nb=8, mb=4, dt=torch.bfloat16, q_stride=None):
+    a = good(B, Hq, Hkv, D, bs, nb, mb, dt)
+    a.update(kc=desc((nb, Hkv, bs, D), torch.uint8), vc=desc((nb, Hkv, bs, D), torch.uint8))
+    if q_stride is not None:
+        a.update(q=desc((B, Hq, D), dt, stride=q_stride))
+    return a
+
+
+def test_fp8_decode_rejects_bad_arguments(lib):
+    assert decode_fp8(lib, **good_fp8(D=64)) == 2                              # head_dim 64
+    assert decode_fp8(lib, **good_fp8(dt=torch.float32)) == 1                  # fp32 queries
+    a = good_fp8()
+    a.update(kc=desc((8, 2, 16, 128), torch.bfloat16))
+    assert decode_fp8(lib, **a) == 1                                           # 16-bit K cache
+    assert decode_fp8(lib, **good_fp8(), ks=0.0) == 1
+    assert decode_fp8(lib, **good_fp8(), vs=float("nan")) == 1
+    assert decode_fp8(lib, **good_fp8(), ks=float("inf")) == 1
+    assert decode_fp8(lib, **good_fp8(q_stride=(4 * 132, 132, 1))) == 2       # rows not 16-byte aligned
+    assert decode_fp8(lib, **good_fp8(B=0)) == 0
+    # the 16-bit entry point refuses E4M3 caches
+    assert decode(lib, **good_fp8()) == 1
+
+
+def test_fp8_append_rejects_bad_arguments(lib):
+    r = ctypes.byref
+    key = desc((3, 2, 128), torch.float16)
+    kc = desc((4, 2, 16, 128), torch.uint8)
+    slots = desc((3,), torch.int64)
+
+    def call(k, v, c1, c2, s, ks=1.0, vs=1.0):
+        return lib.wllm_reshape_and_cache_fp8(r(k), r(v), r(c1), r(c2), r(s), ks, vs, None)
+
+    assert call(key, key, desc((4, 2, 16, 128), torch.float16), kc, slots) == 1    # 16-bit cache
+    assert call(key, desc((3, 2, 128), torch.bfloat16), kc, kc, slots) == 1       # key/value types
+    assert call(key, key, kc, kc, slots, ks=-1.0) == 1
+    assert call(key, key, kc, kc, slots, vs=float("inf")) == 1
+    k6 = desc((3, 2, 6), torch.float16)
+    c6 = desc((4, 2, 16, 6), torch.uint8)
+    assert call(k6, k6, c6, c6, slots) == 2                                         # head_dim % 4
+    empty = desc((0, 2, 128), torch.float16)
+    assert call(empty, empty, kc, kc, desc((0,), torch.int64)) == 0
+    # the bit-copy append refuses E4M3 caches
+    assert lib.wllm_reshape_and_cache(r(key), r(key), r(kc), r(kc), r(slots), None) == 1

@@ -102,6 +102,56 @@ def graph_layers(args, case, dev, q, key, value, slots, bt, cl, flush, stream):
         del pools
 
 
+def fp8_decode(args, case, dev, q, key, value, slots, bt, cl, kc16, vc16, flush, stream):
+    """The same decode step over an fp8 (E4M3) cache: codes drawn from the
+    case's K/V (4x the values, read back with scales 1/4), the decode alone and
+    the fused step timed like the main measurement.  None when the kernel has
+    no fp8 form for this shape (head_dim 64, fp32)."""
+    import paged_kv_cache_185_gb300 as wllm
+
+    if case.dtype == torch.float32 or case.head_dim not in (128, 256) or args.fp8_reps <= 0:
+        return None
+    B, Hkv, bs = case.num_seqs, case.num_kv_heads, case.block_size
+    pools = []
+    for src in (kc16, vc16):  # input codes, drawn on the device block by block (not timed)
+        dst = torch.empty(src.shape, dtype=torch.uint8, device=dev)
+        for i in range(0, src.shape[0], 8192):
+            dst[i:i + 8192] = (src[i:i + 8192].float() * 4.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        pools.append(dst)
+    kc, vc = pools
+    out = torch.empty_like(q)
+    ks = vs = 0.25
+    R = args.fp8_reps
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+        for e in ev:
+            flush.zero_()
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        return sum(e[0].elapsed_time(e[1]) for e in ev) / R
+
+    dec_ms = timed(lambda: wllm.paged_attention_decode_fp8(out, q, kc, vc, bt, cl, Hkv, case.scale, ks, vs, bs))
+    step_ms = timed(lambda: wllm.decode_step_fp8(out, q, key, value, kc, vc, slots, bt, cl, Hkv, case.scale, ks,
+                                                 vs, bs))
+    kv16 = case.kv_bytes_read()
+    alg = case.algorithmic_bytes() - kv16 + kv16 // case.elt  # one byte per cached element
+    peak, peak_kind = measured_peak()
+    achieved = alg / (dec_ms / 1e3) / 1e9
+    del pools, kc, vc
+    return {"kv_dtype": "e4m3", "decode_us": dec_ms * 1e3, "step_us": step_ms * 1e3,
+            "tokens_per_s": B / (step_ms / 1e3), "algorithmic_bytes": alg,
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_persistent<fp8> (decode + in-launch merge)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind},
+            "reps": R, "note": "decode-only and fused-step times over E4M3 caches; L2 flushed between reps"}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -393,6 +443,7 @@ def run_ours(args):
     e2e_value = B * world / (e2e_ms / 1e3)
 
     graph = graph_layers(args, case, dev, q, key, value, slots, bt, cl, flush, stream)
+    fp8 = fp8_decode(args, case, dev, q, key, value, slots, bt, cl, kc, vc, flush, stream)
 
     peak, peak_kind = measured_peak()
     alg = case.algorithmic_bytes()
@@ -426,6 +477,7 @@ def run_ours(args):
         "gpu_launches": K * launches_per_step,
         "clocks": clocks.summary(),
         "graph": graph,
+        "fp8": fp8,
     }
     print(json.dumps(line), flush=True)
 
@@ -437,6 +489,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--graph-layers", type=int, default=8,
                     help="layers per CUDA-graph replay for the graph measurement (0: skip)")
+    ap.add_argument("--fp8-reps", type=int, default=100,
+                    help="repetitions of the fp8-cache measurement (0: skip; head_dim 128/256 only)")
     ap.add_argument("--workload", default="c1", choices=list(workloads.CASE_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -182,12 +182,15 @@ struct Mma<__half> {
 // ---------------------------------------------------------------------------
 // element conversion
 // ---------------------------------------------------------------------------
-// Two E4M3 codes (low byte -> low half) widened to f16x2; exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-  uint32_t y;
-  const uint16_t x = static_cast<uint16_t>(pair16);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));
-  return y;
+// Four E4M3 codes (bytes 0..3) widened to two f16x2: (b0, b1) and (b2, b3);
+// exact.  The register is split into its 16-bit halves in place.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t r, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(r));
 }
 
 // E4M3 codes of (hi, lo): round to nearest even, saturating at +-448.

@@ -102,7 +102,10 @@ constexpr int kMaxGroup = 8;
 constexpr int kPhaseAParts = 2;
 constexpr int kOrderKeys = 36;  // phase-C length buckets 1..32 (0: no phase-C unit), padded
 
-constexpr int kSub = 4;                      // 16-token sub-chunks per stage
+// 16-token sub-chunks per 16-bit stage (64 tokens); the scheduler's work
+// estimates count in these stages.  An fp8 stage holds twice as many
+// sub-chunks in the same bytes (PShape::kSub).
+constexpr int kSub = 4;
 
 // One unit of work: query heads h0 .. h0+nh-1 (kv head kvh, head tile z) of
 // sequence b over tokens [tb, te) of partition `part`.
@@ -145,6 +148,9 @@ struct PShape {
   static constexpr int kHeadTile = 8 * NT;
   using KT = typename std::conditional<F8, uint8_t, T>::type;  // cache element
   static constexpr int kKV = Geom<KT, D>::kTileBytes;  // one 16-row K (or V) sub-tile
+  // sub-chunks per stage: 64 tokens, or 128 over an fp8 cache, where every
+  // consumer warp takes two sub-chunks of a stage as one softmax step
+  static constexpr int kSub = F8 ? 8 : 4;
   static constexpr int kQBytes = kHeadTile * D * static_cast<int>(sizeof(T));
   static constexpr int kStageBytes = ((2 * kSub * kKV + kQBytes) + 1023) / 1024 * 1024;
   // the unit merge writes each consumer's (m, l, O) into the ring slot of
@@ -520,7 +526,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
   constexpr int W = PS::kConsumers;
   constexpr int HT = PS::kHeadTile;
   constexpr int Q = kQueue;
-  constexpr bool kGroupOK = NT == 1 && D <= 128 && !F8;
+  constexpr bool kGroupOK = NT == 1 && D <= 128;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -990,20 +996,22 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       } else {
         const T* qsrc = reinterpret_cast<const T*>(p.q) + cur.b * p.q_sb + static_cast<int64_t>(cur.h0) * p.q_sh;
         const int piece_chunks = min(kPieceChunks, cur.n_chunks - pc0);
-        const int n_stages = (piece_chunks + kSub - 1) / kSub;
+        constexpr int SUB = PS::kSub;
+        static_assert(kPieceChunks % SUB == 0, "a piece is whole stages");
+        const int n_stages = (piece_chunks + SUB - 1) / SUB;
         for (int sg = 0; sg < n_stages; ++sg) {
-          const int c0 = pc0 + sg * kSub;
-          int pbs0[kSub], pbs1[kSub];
+          const int c0 = pc0 + sg * SUB;
+          int pbs0[SUB], pbs1[SUB];
 #pragma unroll
-          for (int j = 0; j < kSub; ++j) {
-            pbs0[j] = __shfl_sync(kFullMask, e0, (sg * kSub + j) & 31);
-            pbs1[j] = __shfl_sync(kFullMask, e1, (sg * kSub + j) & 31);
+          for (int j = 0; j < SUB; ++j) {
+            pbs0[j] = __shfl_sync(kFullMask, e0, (sg * SUB + j) & 31);
+            pbs1[j] = __shfl_sync(kFullMask, e1, (sg * SUB + j) & 31);
           }
           if (!acquire_stage(k)) { ok = false; break; }
           if (lane == 0) {
             const int s = k % S;
             const int t0 = cur.tb + kChunk * c0;
-            const int nsub = min(kSub, cur.n_chunks - c0);
+            const int nsub = min(SUB, cur.n_chunks - c0);
             const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
             const uint32_t bar = smem_u32(full + s);
             const bool first = (pflags & kPieceFirst) && sg == 0;
@@ -1014,7 +1022,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
             const bool two = p.log2_bs < 4;
             uint32_t bytes = 0;
 #pragma unroll
-            for (int j = 0; j < kSub; ++j) {
+            for (int j = 0; j < SUB; ++j) {
               if (j < nsub) {
                 const int tj = t0 + kChunk * j;
                 bytes += (two && !(tj + 8 < cur.te)) ? G::kStageBytes / 2 : G::kStageBytes;
@@ -1024,11 +1032,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
             if (q_rows) bytes += cur.nh * D * static_cast<int>(sizeof(T));
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
-            for (int j = 0; j < kSub; ++j) {
+            for (int j = 0; j < SUB; ++j) {
               if (j < nsub) {
                 const int tj = t0 + kChunk * j;
                 const uint32_t kdst = stage + j * PS::kKV;
-                const uint32_t vdst = stage + (kSub + j) * PS::kKV;
+                const uint32_t vdst = stage + (SUB + j) * PS::kKV;
                 if (!two) {
                   const int y = cur.kvh * p.block_size + (tj & (p.block_size - 1));
 #pragma unroll
@@ -1053,7 +1061,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
             }
             if (q_rows) {
               for (int hh = 0; hh < cur.nh; ++hh)
-                bulk_load(stage + 2 * kSub * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
+                bulk_load(stage + 2 * SUB * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
                           D * static_cast<int>(sizeof(T)), bar);
             }
           }
@@ -1153,19 +1161,29 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
         // state, each stage as two 32-token halves.
         constexpr int kPerWarp = kMaxGroup / W;
         static_assert(kPerWarp * W == kMaxGroup, "group members split evenly over the consumers");
-        MmaState<T, D, kPerWarp> gs;
+        MmaState<MT, D, kPerWarp> gs;
         const int gb = mt_.b, gpart = mt_.p, gh0 = mt_.h0, gnh = mt_.nh, gz = mt_.z;
         const int m0 = kPerWarp * cw;
         const int n_mine = max(0, min(kPerWarp, mt_.group - m0));
-        load_q_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gh0, gnh, lane);
+        if constexpr (F8)
+          load_q_members_e4m3<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gh0, gnh, lane);
+        else
+          load_q_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gh0, gnh, lane);
         int t0 = mt_.t0, tok_end = mt_.tok_end, nsub = mt_.nsub, gflags = mt_.flags;
         for (;;) {
           const uint32_t stg = smem_u32(ring + (k % S) * PS::kStageBytes);
           if (n_mine > 0) {
-            mma_multi<T, D, kPerWarp, 2>(gs, stg, stg + kSub * PS::kKV, t0, tok_end, nsub, p.scale_log2, lane);
-            if (nsub > 2)
-              mma_multi<T, D, kPerWarp, 2>(gs, stg + 2 * PS::kKV, stg + (kSub + 2) * PS::kKV, t0 + 2 * kChunk,
-                                           tok_end, nsub - 2, p.scale_log2, lane);
+            if constexpr (F8) {  // sub-chunk by sub-chunk (the two members give the parallel work)
+#pragma unroll 1
+              for (int qq = 0; qq < nsub; ++qq)
+                mma_chunks_e4m3<D, kPerWarp, 1>(gs, stg + qq * PS::kKV, stg + (PS::kSub + qq) * PS::kKV,
+                                                t0 + qq * kChunk, tok_end, p.scale_log2, lane);
+            } else {
+              mma_multi<T, D, kPerWarp, 2>(gs, stg, stg + kSub * PS::kKV, t0, tok_end, nsub, p.scale_log2, lane);
+              if (nsub > 2)
+                mma_multi<T, D, kPerWarp, 2>(gs, stg + 2 * PS::kKV, stg + (kSub + 2) * PS::kKV, t0 + 2 * kChunk,
+                                             tok_end, nsub - 2, p.scale_log2, lane);
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(empty + k % S));
@@ -1183,22 +1201,31 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
           gflags = gm.flags;
         }
         if (failed) break;
-        finish_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gpart, gh0, gnh, lane);
+        if constexpr (F8)
+          finish_members_e4m3<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gpart, gh0, gnh, lane);
+        else
+          finish_members<T, D, kPerWarp>(gs, p, gb + m0, n_mine, gpart, gh0, gnh, lane);
         if (count_units && !post_done(DoneInfo{gb, gz, mt_.group, 0})) {
           failed = true;
           break;
         }
-        load_q_members<T, D, NT>(st, p, 0, 0, 0, 0, lane);  // the unit state is not carried past a group unit
+        // the unit state is not carried past a group unit
+        if constexpr (F8)
+          load_q_members_e4m3<T, D, NT>(st, p, 0, 0, 0, 0, lane);
+        else
+          load_q_members<T, D, NT>(st, p, 0, 0, 0, 0, lane);
         continue;
       }
     }
     if (!(mt_.flags & kEmptySeq)) {
-      const uint8_t* qtile = ring + s * PS::kStageBytes + 2 * kSub * PS::kKV;
+      const uint8_t* qtile = ring + s * PS::kStageBytes + 2 * PS::kSub * PS::kKV;
       if constexpr (F8) {
+        // consumer cw: sub-chunks 2cw and 2cw + 1 of the 8
+        static_assert(PS::kSub == 2 * W, "two sub-chunks per consumer warp");
         if (mt_.flags & kFirst) load_q_smem_e4m3<T, D, NT>(st, qtile, mt_.nh, lane);
-        if (cw < mt_.nsub)
-          mma_chunk_e4m3<D, NT>(st, stage + cw * PS::kKV, stage + (kSub + cw) * PS::kKV, mt_.t0 + cw * kChunk,
-                                mt_.tok_end, p.scale_log2, lane);
+        if (2 * cw < mt_.nsub)
+          mma_chunks_e4m3<D, NT, 2>(st, stage + 2 * cw * PS::kKV, stage + (PS::kSub + 2 * cw) * PS::kKV,
+                                    mt_.t0 + 2 * cw * kChunk, mt_.tok_end, p.scale_log2, lane);
       } else {
         if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, qtile, mt_.nh, lane);
         if (cw < mt_.nsub)

@@ -119,14 +119,22 @@ def test_fp8_decode_merge_modes(env, monkeypatch):
     assert_attention_close(got, oracle_decode_fp8(case, kc, vc), torch.bfloat16, str(env))
 
 
-def test_fp8_decode_with_shared_prefix_blocks():
+@pytest.mark.parametrize("env", [{}, {"WLLM_PARTITION_TOKENS": "256"}, {"WLLM_PARTITION_TOKENS": "2048"},
+                                 {"WLLM_PREFIX_GROUPS": "0"}, {"WLLM_SEPARATE_COMBINE": "1"}])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_fp8_decode_with_shared_prefix_blocks(env, dtype, monkeypatch):
+    # groups of 8 sequences share 64 blocks (1024 tokens); the last group is
+    # ragged (5 members) and one member ends inside the shared prefix's partition
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
     rng = np.random.default_rng(8)
-    lens = 1024 + rng.integers(1, 3000, size=24)
+    lens = 1024 + rng.integers(1, 3000, size=29)
+    lens[9] = 1024
     case = custom_case("fp8_prefix", lens=lens, num_q_heads=28, num_kv_heads=4, head_dim=128, block_size=16,
-                       dtype=torch.bfloat16, seed=88, groups=(8, 64), append="none")
+                       dtype=dtype, seed=88, groups=(8, 64), append="none")
     kc, vc = fp8_pools(case)
-    got = gpu_decode_fp8(case, kc, vc)
-    assert_attention_close(got, oracle_decode_fp8(case, kc, vc), torch.bfloat16, "shared prefixes")
+    got = gpu_decode_fp8(case, kc, vc, 0.3, 0.7)
+    assert_attention_close(got, oracle_decode_fp8(case, kc, vc, 0.3, 0.7), dtype, f"shared prefixes {env}")
 
 
 def test_fp8_scales_enter_as_binary32_factors():

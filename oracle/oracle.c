@@ -1,6 +1,6 @@
 /*
- * oracle.c -- plain, slow, fp64 CPU reference for the two operations of a
- * paged KV cache decode step:
+ * oracle.c -- plain, slow, fp64 CPU reference for the operations of a paged
+ * KV cache decode step (and the chunked prefill that fills the cache):
  *
  *   1. the KV-cache append ("reshape and cache"): every new token's key and
  *      value vectors are copied, bit for bit, into the physical slot that the
@@ -353,6 +353,111 @@ int oracle_paged_decode_rows(double* out, const int64_t* rows, int64_t n_rows, c
                                      context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                      num_blocks, block_size, max_blocks, scale, dtype, dtype, 1.0f,
                                      1.0f, num_threads);
+}
+
+/*
+ * Chunked-prefill (multi-query) paged attention for a chosen list of output
+ * rows.  Source: the "wLLM" project page, "Features / Core engine" (chunked
+ * prefill: a long prompt enters the cache a chunk at a time, between decode
+ * steps, through the same paged KV cache).  Reading: causal attention, each
+ * chunk token seeing the cached tokens before it and itself.
+ *
+ * q: [T][Hq][D], the chunks of all sequences packed one after another:
+ * sequence b owns q rows query_start_loc[b] .. query_start_loc[b+1]-1 (n_b of
+ * them, n_b may be 0).  Its chunk is the last n_b of its L = context_lens[b]
+ * tokens, whose K/V are already in the cache: chunk token i sits at position
+ * P = L - n_b + i, and for query head h (kv head c = h / G)
+ *   s_j = (double)scale * sum_d q[t][h][d] * K_j[d]   for j = 0 .. P,
+ *   out[t][h][:] = sum_j exp(s_j - m) V_j[:] / sum_j exp(s_j - m),  m = max_j s_j.
+ * rows: indices r = t * Hq + h (NULL: every row in order); out: binary64
+ * [n_rows][D].  Decode is the case n_b = 1.  Inputs are validated first;
+ * nothing is written on error.
+ */
+int oracle_paged_prefill_rows(double* out, const int64_t* rows, int64_t n_rows, const void* q,
+                              const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                              const int32_t* context_lens, const int32_t* query_start_loc,
+                              int64_t num_seqs, int64_t num_tokens, int64_t num_q_heads,
+                              int64_t num_kv_heads, int64_t head_dim, int64_t num_blocks,
+                              int64_t block_size, int64_t max_blocks, float scale, int dtype,
+                              int num_threads) {
+  if (elt_bytes(dtype) == 0 || dtype == ORACLE_E4M3) return ORACLE_BAD_DTYPE;
+  if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      block_size <= 0 || max_blocks < 0 || num_q_heads % num_kv_heads != 0)
+    return ORACLE_BAD_SHAPE;
+  if (rows == NULL && n_rows != num_tokens * num_q_heads) return ORACLE_BAD_SHAPE;
+  if (query_start_loc[0] != 0 || query_start_loc[num_seqs] != num_tokens) return ORACLE_BAD_SHAPE;
+  for (int64_t b = 0; b < num_seqs; ++b) {
+    const int64_t n = (int64_t)query_start_loc[b + 1] - query_start_loc[b];
+    const int64_t L = context_lens[b];
+    if (n < 0) return ORACLE_BAD_SHAPE;
+    if (L < n || L > max_blocks * block_size) return ORACLE_LEN_OUT_OF_RANGE;
+    if (n == 0) continue;
+    for (int64_t jb = 0; jb * block_size < L; ++jb) {
+      const int64_t pb = block_tables[b * max_blocks + jb];
+      if (pb < 0 || pb >= num_blocks) return ORACLE_BLOCK_OUT_OF_RANGE;
+    }
+  }
+  for (int64_t i = 0; i < n_rows; ++i) {
+    const int64_t r = rows ? rows[i] : i;
+    if (r < 0 || r >= num_tokens * num_q_heads) return ORACLE_BAD_SHAPE;
+  }
+  const int64_t G = num_q_heads / num_kv_heads;
+  const double scale_d = (double)scale;
+
+  int status = ORACLE_OK;
+#ifdef _OPENMP
+  if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+  for (int64_t i = 0; i < n_rows; ++i) {
+    const int64_t r = rows ? rows[i] : i;
+    const int64_t t = r / num_q_heads, h = r % num_q_heads;
+    const int64_t c = h / G;
+    /* the sequence owning packed token t: the last b with query_start_loc[b] <= t */
+    int64_t lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) / 2;
+      if (query_start_loc[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t b = lo;
+    const int64_t n = (int64_t)query_start_loc[b + 1] - query_start_loc[b];
+    const int64_t L = context_lens[b];
+    const int64_t P = L - n + (t - query_start_loc[b]); /* this token's position */
+    double* o = out + i * head_dim;
+    for (int64_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+
+    double* s = (double*)malloc((size_t)(P + 1) * sizeof(double));
+    if (s == NULL) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      status = ORACLE_NO_MEMORY;
+      continue;
+    }
+    const int64_t q_off = (t * num_q_heads + h) * head_dim;
+    for (int64_t j = 0; j <= P; ++j) {
+      const int64_t pb = block_tables[b * max_blocks + j / block_size];
+      const int64_t k_off = ((pb * num_kv_heads + c) * block_size + j % block_size) * head_dim;
+      double dot = 0.0;
+      for (int64_t d = 0; d < head_dim; ++d) dot += load_elt(q, q_off + d, dtype) * load_elt(k_cache, k_off + d, dtype);
+      s[j] = scale_d * dot;
+    }
+    double m = s[0];
+    for (int64_t j = 1; j <= P; ++j)
+      if (s[j] > m) m = s[j];
+    double denom = 0.0;
+    for (int64_t j = 0; j <= P; ++j) {
+      const double w = exp(s[j] - m);
+      denom += w;
+      const int64_t pb = block_tables[b * max_blocks + j / block_size];
+      const int64_t v_off = ((pb * num_kv_heads + c) * block_size + j % block_size) * head_dim;
+      for (int64_t d = 0; d < head_dim; ++d) o[d] += w * load_elt(v_cache, v_off + d, dtype);
+    }
+    for (int64_t d = 0; d < head_dim; ++d) o[d] /= denom;
+    free(s);
+  }
+  return status;
 }
 
 /* Number of threads an OpenMP region uses by default (1 without OpenMP). */

@@ -152,6 +152,66 @@ def fp8_decode(args, case, dev, q, key, value, slots, bt, cl, kc16, vc16, flush,
             "reps": R, "note": "decode-only and fused-step times over E4M3 caches; L2 flushed between reps"}
 
 
+def prefill_bench(args, case, dev, flush, stream):
+    """Chunked prefill on the workload's head geometry: 8 sequences, each a
+    512-token chunk after 0..2048 tokens of context (seeded), timed through
+    wllm_paged_attention_prefill.  FLOPs are the causal attention's own
+    (4 * D * (P + 1) per query row at position P), against the measured bf16
+    tensor peak."""
+    import numpy as np
+    import paged_kv_cache_185_gb300 as wllm
+
+    if case.dtype == torch.float32 or case.head_dim not in (64, 128) or args.prefill_reps <= 0:
+        return None
+    rng = np.random.default_rng(77)
+    nseq, chunk = 8, 512
+    prior = rng.integers(0, 2049, size=nseq)
+    lens = [int(x) + chunk for x in prior]
+    pc = workloads.custom_case("prefill", lens=lens, num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                               head_dim=case.head_dim, block_size=case.block_size, dtype=case.dtype, seed=77,
+                               append="none")
+    kc, vc = pc.pool(dev)
+    T = nseq * chunk
+    q = torch.from_numpy(workloads.normal(78, T * case.num_q_heads * case.head_dim)).reshape(
+        T, case.num_q_heads, case.head_dim).to(case.dtype).to(dev)
+    out = torch.empty_like(q)
+    qsl = torch.arange(0, T + 1, chunk, dtype=torch.int32, device=dev)
+    bt, cl = pc.block_tables.to(dev), pc.context_lens.to(dev)
+
+    def call():
+        wllm.paged_attention_prefill(out, q, kc, vc, bt, cl, qsl, case.num_kv_heads, case.scale, case.block_size)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    R = args.prefill_reps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        call()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / R
+    flops = 0
+    for p0 in prior:
+        P = np.arange(int(p0), int(p0) + chunk)
+        flops += int(4 * case.head_dim * (P + 1).sum()) * case.num_q_heads
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (bf16 burst)"
+    except Exception:
+        peak, kind = 1900.0, "fallback"
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"workload": f"{nseq} seqs x {chunk}-token chunks after U[0,2048] context, "
+                        f"{case.num_q_heads}/{case.num_kv_heads} heads, D {case.head_dim}",
+            "us": ms * 1e3, "tokens_per_s": T / (ms / 1e3),
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (mma.sync m16n8k16)",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_kind": kind, "flops": flops},
+            "reps": R}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -444,6 +504,7 @@ def run_ours(args):
 
     graph = graph_layers(args, case, dev, q, key, value, slots, bt, cl, flush, stream)
     fp8 = fp8_decode(args, case, dev, q, key, value, slots, bt, cl, kc, vc, flush, stream)
+    prefill = prefill_bench(args, case, dev, flush, stream)
 
     peak, peak_kind = measured_peak()
     alg = case.algorithmic_bytes()
@@ -478,6 +539,7 @@ def run_ours(args):
         "clocks": clocks.summary(),
         "graph": graph,
         "fp8": fp8,
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
 
@@ -491,6 +553,8 @@ def main():
                     help="layers per CUDA-graph replay for the graph measurement (0: skip)")
     ap.add_argument("--fp8-reps", type=int, default=100,
                     help="repetitions of the fp8-cache measurement (0: skip; head_dim 128/256 only)")
+    ap.add_argument("--prefill-reps", type=int, default=50,
+                    help="repetitions of the chunked-prefill measurement (0: skip)")
     ap.add_argument("--workload", default="c1", choices=list(workloads.CASE_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)

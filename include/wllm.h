@@ -179,6 +179,41 @@ int wllm_decode_step(const wllm_tensor* out, const wllm_tensor* q, const wllm_te
                      const wllm_tensor* context_lens, int num_kv_heads, float scale, int block_size,
                      wllm_stream stream);
 
+/*
+ * Chunked-prefill (multi-query) paged attention.
+ *
+ * Passages: "wLLM" project page, "Features / Core engine" (chunked prefill: a
+ * long prompt enters the paged KV cache a chunk at a time between decode
+ * steps); "mini-vLLM" README, "How it works / Paged KV-cache" (block tables).
+ * Reading (the pages give no formula): causal attention, each chunk token
+ * seeing the sequence's cached tokens before it and itself.
+ *
+ *   out              [T][Hq][D]  written; same type as q; last dim contiguous.
+ *   q                [T][Hq][D]  F16 or BF16; the query chunks of all
+ *                    sequences packed one after another; rows 4-byte aligned.
+ *   k_cache, v_cache [N_b][Hkv][bs][D] dense, same type as q.
+ *   block_tables     [B][M_b] WLLM_I32, last dimension contiguous.
+ *   context_lens     [B] WLLM_I32: L_b, the sequence's tokens in the cache,
+ *                    its chunk included (append the chunk's K/V first).
+ *   query_start_loc  [B+1] WLLM_I32, contiguous: sequence b owns q rows
+ *                    query_start_loc[b] .. query_start_loc[b+1]-1 (n_b of them,
+ *                    0 allowed); query_start_loc[0] = 0, [B] = T, n_b <= L_b.
+ *
+ * Chunk token i of sequence b sits at position P = L_b - n_b + i and
+ *   out[t][h] = sum_{j <= P} softmax_j(scale * q[t][h].k_j) v_j
+ * with query head h reading kv head h / (Hq/Hkv).  A chunk of one token is
+ * the decode.  D 64 or 128; tensor-core products with fp32 accumulation, one
+ * launch, no workspace, no allocation, no host synchronisation (graph
+ * capturable).  Inconsistent query starts or lengths found on the device set
+ * the error word (bit 2) and leave those rows unwritten; in check mode the
+ * call then returns WLLM_ERR_OUT_OF_RANGE.
+ */
+int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q,
+                                 const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                                 const wllm_tensor* block_tables, const wllm_tensor* context_lens,
+                                 const wllm_tensor* query_start_loc, int num_kv_heads,
+                                 float scale, int block_size, wllm_stream stream);
+
 /* ---------------------------------------------------------------------------
  * FP8 (E4M3) KV cache.
  *

@@ -914,6 +914,106 @@ int wllm_decode_step_fp8(const wllm_tensor* out, const wllm_tensor* q, const wll
 }
 
 // ---------------------------------------------------------------------------
+// Chunked-prefill (multi-query) paged attention.
+// ---------------------------------------------------------------------------
+int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                 const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                 const wllm_tensor* context_lens, const wllm_tensor* query_start_loc,
+                                 int num_kv_heads, float scale, int block_size, wllm_stream stream) {
+  int rc;
+  if ((rc = check_desc(out, "out", 3)) || (rc = check_desc(q, "q", 3)) ||
+      (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
+      (rc = check_desc(block_tables, "block_tables", 2)) || (rc = check_desc(context_lens, "context_lens", 1)) ||
+      (rc = check_desc(query_start_loc, "query_start_loc", 1)))
+    return rc;
+  const int dt = q->dtype;
+  if (dt != WLLM_F16 && dt != WLLM_BF16) return fail(WLLM_ERR_UNSUPPORTED, "prefill takes F16 or BF16 inputs");
+  if (out->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
+    return fail(WLLM_ERR_INVALID_ARG, "q, out and caches must share one dtype");
+  if (block_tables->dtype != WLLM_I32 || context_lens->dtype != WLLM_I32 || query_start_loc->dtype != WLLM_I32)
+    return fail(WLLM_ERR_INVALID_ARG, "block_tables, context_lens and query_start_loc must be I32");
+  if (!same_shape(out, q)) return fail(WLLM_ERR_INVALID_ARG, "out and q shapes differ");
+  if (!same_shape(k_cache, v_cache)) return fail(WLLM_ERR_INVALID_ARG, "k_cache and v_cache shapes differ");
+  const int64_t T = q->shape[0], hq = q->shape[1], d = q->shape[2];
+  const int64_t nb = k_cache->shape[0], hkv = k_cache->shape[1], bs = k_cache->shape[2];
+  const int64_t B = context_lens->shape[0], mb = block_tables->shape[1];
+  if (k_cache->shape[3] != d) return fail(WLLM_ERR_INVALID_ARG, "cache head_dim differs from q");
+  if (hkv != num_kv_heads)
+    return fail(WLLM_ERR_INVALID_ARG, "num_kv_heads %d differs from cache dim %lld", num_kv_heads, (long long)hkv);
+  if (bs != block_size)
+    return fail(WLLM_ERR_INVALID_ARG, "block_size %d differs from cache dim %lld", block_size, (long long)bs);
+  if (hkv <= 0 || hq % hkv != 0) return fail(WLLM_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  if (block_tables->shape[0] != B) return fail(WLLM_ERR_INVALID_ARG, "block_tables must have B rows");
+  if (query_start_loc->shape[0] != B + 1) return fail(WLLM_ERR_INVALID_ARG, "query_start_loc must have B+1 entries");
+  if (B > 1 && context_lens->stride[0] != 1) return fail(WLLM_ERR_INVALID_ARG, "context_lens must be contiguous");
+  if (query_start_loc->stride[0] != 1) return fail(WLLM_ERR_INVALID_ARG, "query_start_loc must be contiguous");
+  if (mb > 1 && block_tables->stride[1] != 1)
+    return fail(WLLM_ERR_INVALID_ARG, "block_tables rows must be contiguous");
+  if (!contiguous(k_cache) || !contiguous(v_cache)) return fail(WLLM_ERR_INVALID_ARG, "caches must be dense");
+  if (d > 1 && (q->stride[2] != 1 || out->stride[2] != 1))
+    return fail(WLLM_ERR_INVALID_ARG, "q/out last dimension must be contiguous");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(WLLM_ERR_INVALID_ARG, "scale must be finite");
+  if (d != 64 && d != 128) return fail(WLLM_ERR_UNSUPPORTED, "prefill head_dim %lld not supported (64, 128)", (long long)d);
+  if (!is_pow2(bs) || bs < 8 || bs > 256)
+    return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
+  if (T > INT32_MAX / 64 || B > INT32_MAX / 2 || hq > 65535 || hkv > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
+    return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
+  if (T == 0 || B == 0 || hq == 0) return WLLM_OK;
+  if (nb < 1) return fail(WLLM_ERR_INVALID_ARG, "the pool has no blocks");
+  if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
+    return fail(WLLM_ERR_INVALID_ARG, "cache base pointers must be 16-byte aligned");
+  if (!(aligned(q->data, 4) && aligned(out->data, 4) && q->stride[0] % 2 == 0 && q->stride[1] % 2 == 0 &&
+        out->stride[0] % 2 == 0 && out->stride[1] % 2 == 0))
+    return fail(WLLM_ERR_INVALID_ARG, "q/out rows must be 4-byte aligned");
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* s = nullptr;
+  if ((rc = device_state(&s))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap kmap, vmap;
+  if ((rc = make_pool_map(&kmap, k_cache->data, dt, nb, hkv, bs, d, "k_cache"))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, dt, nb, hkv, bs, d, "v_cache"))) return rc;
+  const bool check = env_flag("WLLM_CHECK");
+  if (check) {
+    cudaError_t e = static_cast<cudaError_t>(launch_check_decode(
+        static_cast<const int32_t*>(block_tables->data), block_tables->stride[0],
+        static_cast<const int32_t*>(context_lens->data), static_cast<int>(B), static_cast<int>(mb),
+        static_cast<int>(bs), static_cast<int>(nb), s->err, st));
+    if (e != cudaSuccess) return cuda_fail(e, "check_decode launch");
+    if ((rc = collect_device_errors(s, st, "paged_attention_prefill"))) return rc;
+  }
+  PrefillParams p{};
+  p.out = out->data;
+  p.q = q->data;
+  p.q_st = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.o_st = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_stride = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.query_start_loc = static_cast<const int32_t*>(query_start_loc->data);
+  p.num_seqs = static_cast<int>(B);
+  p.num_tokens = static_cast<int>(T);
+  p.num_q_heads = static_cast<int>(hq);
+  p.num_kv_heads = static_cast<int>(hkv);
+  p.group = static_cast<int>(hq / hkv);
+  p.max_blocks = static_cast<int>(mb);
+  p.block_size = static_cast<int>(bs);
+  p.log2_bs = ilog2(bs);
+  p.num_blocks = static_cast<int>(nb);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = s->err;
+  p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
+  const int grid_x = prefill_grid_x(T, B, p.group);
+  cudaError_t e = static_cast<cudaError_t>(launch_prefill(dt, static_cast<int>(d), kmap, vmap, p, grid_x, st));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  if (check) return collect_device_errors(s, st, "paged_attention_prefill");
+  return WLLM_OK;
+}
+
+// ---------------------------------------------------------------------------
 // Allocation-free decode.
 //
 // Some callers cannot let a library allocate device memory: a caller that is

@@ -80,6 +80,30 @@ constexpr int kPersistentMaxParts = 256;      // partitions per sequence (the ho
 
 int launch_append(const AppendParams& p, cudaStream_t stream);
 
+// Chunked-prefill (multi-query) paged attention: q/out [T][Hq][D] packed by
+// sequence (query_start_loc [B+1]); each chunk is the last n_b of the
+// sequence's context_lens[b] tokens and attends causally.
+struct PrefillParams {
+  void* out;
+  const void* q;
+  int64_t q_st, q_sh;             // q strides (elements) of the token and head dims
+  int64_t o_st, o_sh;             // out strides
+  const int32_t* block_tables;
+  int64_t bt_stride;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int num_seqs, num_tokens, num_q_heads, num_kv_heads, group;
+  int max_blocks, block_size, log2_bs, num_blocks;
+  float scale_log2;               // scale * log2(e)
+  int* err;
+  unsigned long long wait_limit_ns;
+};
+// CTAs along x for T packed tokens of B sequences (grid y = kv heads).
+int prefill_grid_x(int64_t num_tokens, int64_t num_seqs, int group);
+// f16/bf16 (dtype code 1/2), head_dim 64 or 128; returns a cudaError_t value.
+int launch_prefill(int dtype, int head_dim, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                   const PrefillParams& p, int grid_x, cudaStream_t stream);
+
 // Check-mode kernels: record index errors in the device error word.
 int launch_check_decode(const int32_t* block_tables, int64_t bt_stride,
                         const int32_t* context_lens, int num_seqs, int max_blocks,

@@ -1,0 +1,124 @@
+"""Chunked-prefill paged attention on the GPU, through the C ABI, against the
+oracle: packed query chunks (fresh prompts, continued prompts, one-token and
+empty chunks), GQA/MHA, head dims 64/128, block sizes 8..64, and a large
+sampled case."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_185_gb300 as wllm
+from paged_kv_cache_185_gb300.workloads import custom_case
+from tests.gpu_common import assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_case(lens, chunks, Hq, Hkv, D, bs, dtype, seed):
+    """Pools holding every sequence's L tokens (the chunk's K/V appended) and packed query chunks."""
+    case = custom_case("prefill", lens=lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                       dtype=dtype, seed=seed, spare_blocks=2, append="none")
+    gen = torch.Generator().manual_seed(seed + 7)
+    T = int(sum(chunks))
+    q = torch.randn(T, Hq, D, generator=gen).to(dtype)
+    qsl = torch.tensor(np.concatenate([[0], np.cumsum(chunks)]), dtype=torch.int32)
+    return case, q, qsl
+
+
+def run_gpu(case, q, qsl, out=None):
+    dev = "cuda"
+    kc, vc = case.pool(dev)
+    qd = q.to(dev)
+    o = torch.empty_like(qd) if out is None else out
+    wllm.paged_attention_prefill(o, qd, kc, vc, case.block_tables.to(dev), case.context_lens.to(dev), qsl.to(dev),
+                                 case.num_kv_heads, case.scale, case.block_size)
+    torch.cuda.synchronize()
+    return o.cpu()
+
+
+def run_oracle(case, q, qsl, rows=None):
+    kc, vc = case.pool("cpu")
+    return oracle.paged_prefill(q, kc, vc, case.block_tables, case.context_lens, qsl, case.num_kv_heads,
+                                case.scale, rows=rows)
+
+
+CASES = [
+    # (Hq, Hkv, D, bs, lens, chunks)
+    (8, 8, 128, 16, [200, 64, 1, 77, 500, 33], [200, 64, 1, 13, 129, 0]),    # MHA: fresh, continued, 1, 0
+    (32, 8, 128, 16, [300, 1000, 17, 65], [300, 255, 17, 1]),                 # GQA 4
+    (28, 4, 128, 32, [513, 90, 1200], [513, 90, 70]),                         # GQA 7, bs 32
+    (12, 1, 64, 8, [100, 257, 31], [100, 200, 9]),                            # MQA, D 64, bs 8
+    (16, 2, 64, 64, [640, 1, 129], [128, 1, 129]),                            # D 64, bs 64
+    (64, 4, 128, 16, [150, 333], [150, 20]),                                  # GQA 16
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,lens,chunks", CASES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_prefill_matches_oracle(Hq, Hkv, D, bs, lens, chunks, dtype):
+    case, q, qsl = prefill_case(lens, chunks, Hq, Hkv, D, bs, dtype, seed=Hq * 3 + D + bs)
+    got = run_gpu(case, q, qsl)
+    ref = run_oracle(case, q, qsl)
+    assert_attention_close(got, ref, dtype, f"prefill {Hq}/{Hkv} D{D} bs{bs}")
+
+
+def test_prefill_one_token_chunks_match_decode():
+    # n_b = 1 everywhere: the decode's answer
+    rng = np.random.default_rng(2)
+    lens = rng.integers(1, 3000, size=20)
+    case, q, qsl = prefill_case(lens, [1] * 20, 28, 4, 128, 16, torch.bfloat16, seed=21)
+    got = run_gpu(case, q, qsl)
+    dev = "cuda"
+    kc, vc = case.pool(dev)
+    dec = torch.empty(20, 28, 128, dtype=torch.bfloat16, device=dev)
+    wllm.paged_attention_decode(dec, q.to(dev), kc, vc, case.block_tables.to(dev), case.context_lens.to(dev), 4,
+                                case.scale, 16)
+    ref = run_oracle(case, q, qsl)
+    assert_attention_close(got, ref, torch.bfloat16, "prefill n=1")
+    assert_attention_close(dec.cpu(), ref, torch.bfloat16, "decode")
+
+
+def test_prefill_strided_output_and_query():
+    # q and out as slices of wider buffers (a fused QKV projection and a padded output)
+    case, q, qsl = prefill_case([90, 40], [90, 15], 8, 2, 64, 16, torch.float16, seed=31)
+    dev = "cuda"
+    wide_q = torch.zeros(q.shape[0], 12, 64, dtype=q.dtype, device=dev)
+    wide_q[:, 2:10] = q.to(dev)
+    wide_o = torch.full((q.shape[0], 10, 64), 7.0, dtype=q.dtype, device=dev)
+    kc, vc = case.pool(dev)
+    wllm.paged_attention_prefill(wide_o[:, 1:9], wide_q[:, 2:10], kc, vc, case.block_tables.to(dev),
+                                 case.context_lens.to(dev), qsl.to(dev), 2, case.scale, 16)
+    torch.cuda.synchronize()
+    assert_attention_close(wide_o[:, 1:9].cpu(), run_oracle(case, q, qsl), torch.float16, "strided")
+    assert (wide_o[:, 0] == 7).all() and (wide_o[:, 9] == 7).all()
+
+
+def test_prefill_long_chunks_sampled():
+    # four sequences, 1024-token chunks after 0..3000 tokens of context: sampled rows
+    rng = np.random.default_rng(4)
+    prior = rng.integers(0, 3000, size=4)
+    chunks = [1024] * 4
+    lens = [int(p) + 1024 for p in prior]
+    case, q, qsl = prefill_case(lens, chunks, 32, 8, 128, 16, torch.bfloat16, seed=41)
+    got = run_gpu(case, q, qsl)
+    rows = np.sort(rng.choice(q.shape[0] * 32, size=256, replace=False))
+    ref = run_oracle(case, q, qsl, rows=torch.from_numpy(rows))
+    assert_attention_close(got.reshape(-1, 128)[torch.from_numpy(rows)], ref, torch.bfloat16, "long chunks")
+
+
+def test_prefill_reports_inconsistent_query_starts(monkeypatch):
+    monkeypatch.setenv("WLLM_CHECK", "1")
+    case, q, qsl = prefill_case([40, 40], [20, 20], 8, 2, 64, 16, torch.bfloat16, seed=51)
+    bad = qsl.clone()
+    bad[1] = 30  # sequence 0 now claims 30 query rows ...
+    cl = case.context_lens.clone()
+    cl[0] = 25  # ... but holds 25 tokens: a chunk longer than its context
+    dev = "cuda"
+    kc, vc = case.pool(dev)
+    out = torch.zeros(q.shape, dtype=q.dtype, device=dev)
+    with pytest.raises(wllm.WllmError):
+        wllm.paged_attention_prefill(out, q.to(dev), kc, vc, case.block_tables.to(dev), cl.to(dev), bad.to(dev), 2,
+                                     case.scale, 16)
+    assert wllm.device_errors() == 0  # the failing call cleared the word

@@ -1,5 +1,8 @@
 // decode_persistent.cuh -- persistent, warp-specialised paged decode for
-// f16/bf16 (tensor-core QK^T and PV), sm_103a.
+// f16/bf16 queries (tensor-core QK^T and PV), sm_103a, over a 16-bit cache or
+// (F8 instantiations) an E4M3 cache with per-tensor K/V scales: the same
+// schedule and pipeline, 128-token stages of codes widened in registers
+// (mma_e4m3.cuh), each consumer warp taking two 16-token sub-chunks.
 //
 // Work is cut into units (sequence b, kv-head tile z, partition p of P tokens).
 // The grid is two CTAs per SM (one for head_dim 256); each CTA loops until the

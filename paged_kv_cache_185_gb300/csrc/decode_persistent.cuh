@@ -152,7 +152,9 @@ struct PShape {
   using KT = typename std::conditional<F8, uint8_t, T>::type;  // cache element
   static constexpr int kKV = Geom<KT, D>::kTileBytes;  // one 16-row K (or V) sub-tile
   // sub-chunks per stage: 64 tokens, or 128 over an fp8 cache, where every
-  // consumer warp takes two sub-chunks of a stage as one softmax step
+  // consumer warp takes two sub-chunks of a stage as one softmax step (tried
+  // for 16-bit head_dim 64 too: no faster, the TinyLlama-shaped batch is bound
+  // by start-up and tail, not by the consumers' issue rate)
   static constexpr int kSub = F8 ? 8 : 4;
   static constexpr int kQBytes = kHeadTile * D * static_cast<int>(sizeof(T));
   static constexpr int kStageBytes = ((2 * kSub * kKV + kQBytes) + 1023) / 1024 * 1024;
@@ -1181,11 +1183,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
               for (int qq = 0; qq < nsub; ++qq)
                 mma_chunks_e4m3<D, kPerWarp, 1>(gs, stg + qq * PS::kKV, stg + (PS::kSub + qq) * PS::kKV,
                                                 t0 + qq * kChunk, tok_end, p.scale_log2, lane);
-            } else {
-              mma_multi<T, D, kPerWarp, 2>(gs, stg, stg + kSub * PS::kKV, t0, tok_end, nsub, p.scale_log2, lane);
-              if (nsub > 2)
-                mma_multi<T, D, kPerWarp, 2>(gs, stg + 2 * PS::kKV, stg + (kSub + 2) * PS::kKV, t0 + 2 * kChunk,
-                                             tok_end, nsub - 2, p.scale_log2, lane);
+            } else {  // the stage as 32-token pieces
+#pragma unroll 1
+              for (int qq = 0; qq < nsub; qq += 2)
+                mma_multi<T, D, kPerWarp, 2>(gs, stg + qq * PS::kKV, stg + (PS::kSub + qq) * PS::kKV,
+                                             t0 + qq * kChunk, tok_end, nsub - qq, p.scale_log2, lane);
             }
           }
           __syncwarp();
@@ -1231,9 +1233,15 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
                                     mt_.t0 + 2 * cw * kChunk, mt_.tok_end, p.scale_log2, lane);
       } else {
         if (mt_.flags & kFirst) load_q_smem<T, D, NT>(st, qtile, mt_.nh, lane);
-        if (cw < mt_.nsub)
-          mma_chunk<T, D, NT>(st, stage + cw * PS::kKV, stage + (kSub + cw) * PS::kKV, mt_.t0 + cw * kChunk,
-                              mt_.tok_end, p.scale_log2, lane);
+        if constexpr (PS::kSub == 2 * W) {  // consumer cw: sub-chunks 2cw and 2cw + 1
+          if (2 * cw < mt_.nsub)
+            mma_multi<T, D, NT, 2>(st, stage + 2 * cw * PS::kKV, stage + (PS::kSub + 2 * cw) * PS::kKV,
+                                   mt_.t0 + 2 * cw * kChunk, mt_.tok_end, mt_.nsub - 2 * cw, p.scale_log2, lane);
+        } else {
+          if (cw < mt_.nsub)
+            mma_chunk<T, D, NT>(st, stage + cw * PS::kKV, stage + (PS::kSub + cw) * PS::kKV,
+                                mt_.t0 + cw * kChunk, mt_.tok_end, p.scale_log2, lane);
+        }
       }
     }
     __syncwarp();

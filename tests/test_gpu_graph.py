@@ -82,3 +82,54 @@ def test_decode_step_graph_replay(monkeypatch, dtype, Hq, Hkv, D, part):
         assert_attention_close(xs[0]["out"].cpu(), ref, dtype, "graph layer 0")
     finally:
         wllm.set_workspace(None)
+
+
+def test_fp8_step_and_prefill_graph_replay():
+    # the fp8 fused step (two layers) and a chunked prefill, captured in one graph
+    cases = _layers(2, torch.bfloat16, 32, 8, 128)
+    xs = []
+    for c in cases:
+        x = _inputs(c)
+        kh, vh = c.pool("cpu")
+        x["kc"], x["vc"] = workloads.e4m3_codes(kh, 4.0).cuda(), workloads.e4m3_codes(vh, 4.0).cuda()
+        xs.append(x)
+    pc = workloads.custom_case("graph_prefill", lens=[300, 1500], num_q_heads=28, num_kv_heads=4, head_dim=128,
+                               block_size=16, dtype=torch.bfloat16, seed=77, append="none")
+    pk, pv = pc.pool("cuda")
+    pq = torch.randn(700, 28, 128, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
+    pqsl = torch.tensor([0, 300, 700], dtype=torch.int32, device="cuda")
+    pbt, pcl = pc.block_tables.cuda(), pc.context_lens.cuda()
+    pout = torch.empty_like(pq)
+
+    def run():
+        for c, x in zip(cases, xs):
+            wllm.decode_step_fp8(x["out"], x["q"], x["key"], x["value"], x["kc"], x["vc"], x["slots"], x["bt"],
+                                 x["cl"], c.num_kv_heads, c.scale, 0.25, 0.25, c.block_size)
+        wllm.paged_attention_prefill(pout, pq, pk, pv, pbt, pcl, pqsl, 4, pc.scale, 16)
+
+    need = max(wllm.workspace_bytes(c.num_seqs, c.num_q_heads, c.num_kv_heads, c.head_dim, c.max_blocks,
+                                    c.block_size) for c in cases)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    wllm.set_workspace(ws)
+    try:
+        run()
+        torch.cuda.synchronize()
+        eager = [x["out"].clone() for x in xs] + [pout.clone()]
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            run()
+        for t in [x["out"] for x in xs] + [pout]:
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert wllm.device_errors() == 0
+        for t, e in zip([x["out"] for x in xs] + [pout], eager):
+            assert torch.equal(int_view(t), int_view(e)), "replay differs from eager"
+    finally:
+        wllm.set_workspace(None)

@@ -30,6 +30,7 @@ namespace {
 constexpr int kPfRows = 64;      // query rows per CTA
 constexpr int kPfWarps = 4;      // consumer warps (16 rows each)
 constexpr int kPfKv = 64;        // kv tokens per stage
+constexpr int kPfStep = 32;      // kv tokens per softmax step (a divisor of kPfKv; 64 measured slower)
 constexpr int kPfThreads = (kPfWarps + 1) * 32;
 
 template <typename T, int D>
@@ -252,33 +253,35 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     if (warp_live && t0 <= warp_pmax) {
       const uint32_t kt = smem_u32(ring + s * PS::kStageBytes);
       const uint32_t vt = kt + 4 * PS::kSub;
-      // the stage as two 32-token softmax steps (sub-tiles 2h and 2h + 1)
+      // the stage as kPfKv / kPfStep softmax steps
+      constexpr int NJ = kPfStep / 16;  // 16-token sub-tiles per step
+      constexpr int NN = kPfStep / 8;   // 8-token n-tiles per step
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int th = t0 + 32 * h;
+      for (int h = 0; h < kPfKv / kPfStep; ++h) {
+        const int th = t0 + kPfStep * h;
         if (th > warp_pmax) break;
-        // S = Q K^T over 32 tokens: n-tile nt covers tokens th + 8nt .. th + 8nt + 7
-        float sc[4][4];
+        // S = Q K^T over the step: n-tile nt covers tokens th + 8nt .. th + 8nt + 7
+        float sc[NN][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < NN; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
+          for (int j = 0; j < NJ; ++j) {
             uint32_t r[4];
-            ldsm_x4(kt + (2 * h + j) * PS::kSub + tile_offset(kb_row, 2 * ks + kb_chunk), r);
+            ldsm_x4(kt + (NJ * h + j) * PS::kSub + tile_offset(kb_row, 2 * ks + kb_chunk), r);
             const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
             Mma<T>::run(sc[2 * j], qa[ks], b0);
             Mma<T>::run(sc[2 * j + 1], qa[ks], b1);
           }
         }
-        // causal mask where the 32 tokens reach past a row's position (and past kv_end)
-        const bool masked = th + 31 > warp_pmin;
+        // causal mask where the step reaches past a row's position (and past kv_end)
+        const bool masked = th + kPfStep - 1 > warp_pmin;
         float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < NN; ++nt) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int tok = th + nt * 8 + 2 * c + e;
@@ -302,10 +305,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const float al_a = exp2f(m_a - mn_a), al_b = exp2f(m_b - mn_b);
         m_a = mn_a;
         m_b = mn_b;
-        uint32_t pa_frag[2][4];  // P as A fragments of the two 16-token k steps
+        uint32_t pa_frag[NJ][4];  // P as A fragments of the step's 16-token k steps
         float sum_a = 0.f, sum_b = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < NN; ++nt) {
           const float p0 = exp2f(sc[nt][0] - mn_a), p1 = exp2f(sc[nt][1] - mn_a);
           const float p2 = exp2f(sc[nt][2] - mn_b), p3 = exp2f(sc[nt][3] - mn_b);
           sum_a += p0 + p1;
@@ -325,9 +328,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           }
         }
         // O += P V; V rows at or past kv_end were not staged this time: zero them
-        const bool tail = th + 32 > kv_end;
+        const bool tail = th + kPfStep > kv_end;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < NJ; ++j) {
           uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
           if (tail) {
             const int tk = th + 16 * j + 2 * c;
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 #pragma unroll
           for (int dp = 0; dp < D / 16; ++dp) {
             uint32_t r[4];
-            ldsm_x4_trans(vt + (2 * h + j) * PS::kSub + tile_offset(vb_row, 2 * dp + vb_chunk), r);
+            ldsm_x4_trans(vt + (NJ * h + j) * PS::kSub + tile_offset(vb_row, 2 * dp + vb_chunk), r);
             const uint32_t b0[2] = {r[0] & keep0, r[1] & keep1}, b1[2] = {r[2] & keep0, r[3] & keep1};
             Mma<T>::run(o[2 * dp], pa_frag[j], b0);
             Mma<T>::run(o[2 * dp + 1], pa_frag[j], b1);

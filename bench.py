@@ -18,6 +18,11 @@ With N > 1 (torchrun), every rank runs its own replica of the workload with its
 own seed (sequences are independent: no collective on the data path); rank 0
 prints one JSON line with the whole-job tokens/s over the slowest rank's time.
 
+Extra fields of the line: "graph" (several layers' steps replayed from one CUDA
+graph vs issued eagerly), "fp8" (the same decode and step over an E4M3 cache,
+head_dim 128/256 workloads) and "prefill" (chunked-prefill paged attention on
+the workload's head geometry, against the measured bf16 tensor peak).
+
 --impl reference times the fp64 CPU oracle on the host cores, on a bounded
 sample of the same workload (rank 0 only).
 """

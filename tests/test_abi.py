@@ -167,3 +167,36 @@ def test_fp8_append_rejects_bad_arguments(lib):
     assert call(empty, empty, kc, kc, desc((0,), torch.int64)) == 0
     # the bit-copy append refuses E4M3 caches
     assert lib.wllm_reshape_and_cache(r(key), r(key), r(kc), r(kc), r(slots), None) == 1
+
+
+def prefill(lib, out, q, kc, vc, bt, cl, qsl, hkv=2, scale=0.125, bs=16):
+    r = lambda x: None if x is None else ctypes.byref(x)  # noqa: E731
+    return lib.wllm_paged_attention_prefill(r(out), r(q), r(kc), r(vc), r(bt), r(cl), r(qsl), hkv, scale, bs, None)
+
+
+def good_prefill(T=10, B=2, Hq=4, Hkv=2, D=64, bs=16, nb=8, mb=4, dt=torch.bfloat16):
+    a = good(B, Hq, Hkv, D, bs, nb, mb, dt)
+    a.update(out=desc((T, Hq, D), dt), q=desc((T, Hq, D), dt), qsl=desc((B + 1,), torch.int32))
+    return a
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    assert prefill(lib, **good_prefill(D=256)) == 2                     # head_dim 256
+    assert prefill(lib, **good_prefill(dt=torch.float32)) == 2          # fp32
+    a = good_prefill()
+    a.update(qsl=desc((2,), torch.int32))                               # B entries, not B + 1
+    assert prefill(lib, **a) == 1
+    a = good_prefill()
+    a.update(qsl=desc((3,), torch.int64))                               # dtype
+    assert prefill(lib, **a) == 1
+    a = good_prefill()
+    a.update(kc=desc((8, 2, 16, 64), torch.float16))                    # cache dtype
+    assert prefill(lib, **a) == 1
+    assert prefill(lib, **good_prefill(), hkv=3) == 1                   # kv heads mismatch
+    assert prefill(lib, **good_prefill(), bs=8) == 1                    # block size mismatch
+    assert prefill(lib, **good_prefill(bs=4), bs=4) == 2                # unsupported block size
+    assert prefill(lib, **good_prefill(), scale=float("inf")) == 1
+    a = good_prefill()
+    a.update(q=desc((10, 4, 64), torch.bfloat16, stride=(257, 64, 1)))  # rows not 4-byte aligned
+    assert prefill(lib, **a) == 1
+    assert prefill(lib, **good_prefill(T=0)) == 0                       # nothing to do

@@ -19,8 +19,8 @@ own seed (sequences are independent: no collective on the data path); rank 0
 prints one JSON line with the whole-job tokens/s over the slowest rank's time.
 
 Extra fields of the line: "graph" (several layers' steps replayed from one CUDA
-graph vs issued eagerly), "fp8" (the same decode and step over an E4M3 cache,
-head_dim 128/256 workloads) and "prefill" (chunked-prefill paged attention on
+graph vs issued eagerly), "fp8" (the same decode and step over an E4M3 cache)
+and "prefill" (chunked-prefill paged attention on
 the workload's head geometry, against the measured bf16 tensor peak).
 
 --impl reference times the fp64 CPU oracle on the host cores, on a bounded
@@ -111,10 +111,11 @@ def fp8_decode(args, case, dev, q, key, value, slots, bt, cl, kc16, vc16, flush,
     """The same decode step over an fp8 (E4M3) cache: codes drawn from the
     case's K/V (4x the values, read back with scales 1/4), the decode alone and
     the fused step timed like the main measurement.  None when the kernel has
-    no fp8 form for this shape (head_dim 64, fp32)."""
+    no fp8 form for this shape (fp32 queries, head_dim 64 with 8-token blocks)."""
     import paged_kv_cache_185_gb300 as wllm
 
-    if case.dtype == torch.float32 or case.head_dim not in (128, 256) or args.fp8_reps <= 0:
+    if (case.dtype == torch.float32 or case.head_dim not in (64, 128, 256) or args.fp8_reps <= 0
+            or (case.head_dim == 64 and case.block_size < 16)):
         return None
     B, Hkv, bs = case.num_seqs, case.num_kv_heads, case.block_size
     pools = []

@@ -247,12 +247,12 @@ int wllm_reshape_and_cache_fp8(const wllm_tensor* key, const wllm_tensor* value,
  * Paged decode attention over E4M3 caches:
  *   out[b][h] = sum_j softmax_j(scale * q.(k_scale * K_j)) * (v_scale * V_j)
  * with K_j, V_j the dequantised codes.  q and out F16 or BF16 (one type),
- * query rows 16-byte aligned; D 128 or 256.  The codes are widened to f16
- * exactly on the device; bf16 queries are rounded to f16 for the tensor-core
- * products (|q| must stay within the f16 range); accumulation is fp32.  Runs
- * the persistent kernel with split-KV merged inside the launch, like
- * wllm_paged_attention_decode (same workspace rules, graph-capturable with a
- * caller workspace); shared-prefix grouping is not used.
+ * query rows 16-byte aligned; D 64 (block_size >= 16), 128 or 256.  The codes
+ * are widened to f16 exactly on the device; bf16 queries are rounded to f16 for
+ * the tensor-core products (|q| must stay within the f16 range); accumulation
+ * is fp32.  Runs the persistent kernel with split-KV merged inside the launch,
+ * like wllm_paged_attention_decode (same workspace rules, graph-capturable with
+ * a caller workspace, shared prompt prefixes read once per group for D <= 128).
  */
 int wllm_paged_attention_decode_fp8(const wllm_tensor* out, const wllm_tensor* q,
                                     const wllm_tensor* k_cache, const wllm_tensor* v_cache,

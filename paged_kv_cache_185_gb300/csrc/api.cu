@@ -279,6 +279,14 @@ int make_pool_map(CUtensorMap* map, const void* base, int dtype, int64_t num_blo
                         static_cast<cuuint64_t>(num_blocks)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elt), static_cast<cuuint64_t>(hkv * bs * d * elt)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(bs < 16 ? bs : 16), 1};
+  if (dtype == WLLM_FP8_E4M3 && d == 64) {
+    // 64-byte rows of codes: view the pool as rows of two tokens (128 bytes),
+    // 16 tokens being one box of 8 such rows (block_size >= 16, checked)
+    dims[0] = 128;
+    dims[1] = static_cast<cuuint64_t>(hkv * bs / 2);
+    strides[0] = 128;
+    box[1] = 8;
+  }
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -556,7 +564,7 @@ size_t wllm_paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int n
       need = std::max(need, pl.counter_bytes + pl.ml_bytes + pl.o_bytes);
     }
   }
-  if (head_dim == 128 || head_dim == 256) {  // decode over an fp8 cache
+  {  // decode over an fp8 cache
     const int64_t B = std::min<int64_t>(num_seqs, kPersistentMaxSeqs);
     const DecodePlan pl = make_plan(WLLM_BF16, B, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                     block_size, true, sms, true);
@@ -720,7 +728,8 @@ int prepare_decode(const wllm_tensor* out, const wllm_tensor* q, const wllm_tens
     return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
   if (B > INT32_MAX || hq > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
     return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
-  if (kv_fp8 && d == 64) return fail(WLLM_ERR_UNSUPPORTED, "an fp8 cache needs head_dim 128 or 256");
+  if (kv_fp8 && d == 64 && bs < 16)
+    return fail(WLLM_ERR_UNSUPPORTED, "an fp8 cache with head_dim 64 needs block_size >= 16");
   a = DecodeArgs{};
   a.kv_dt = kv_fp8 ? WLLM_FP8_E4M3 : dt;
   a.kv_fp8 = kv_fp8;

@@ -47,7 +47,22 @@ struct Geom {
   static constexpr int kColBoxes = D / kBoxCols;       // boxes across a row of D elements
   static constexpr int kTileBytes = kColBoxes * 2048;  // 16 rows of one head's K (or V)
   static constexpr int kStageBytes = 2 * kTileBytes;   // K tile then V tile
+  static constexpr bool kPairRows = false;
   static_assert(D % kBoxCols == 0, "head_dim must fill whole 128-byte rows");
+};
+
+// E4M3 codes with head_dim 64: a token row is 64 bytes, so the pool is viewed
+// as rows of two tokens (128 bytes, still one swizzled box row); 16 tokens are
+// one box of 8 such rows.  Token r of a tile sits in box row r / 2, bytes
+// 64 (r % 2) .. 64 (r % 2) + 63.
+template <>
+struct Geom<uint8_t, 64> {
+  static constexpr int kElt = 1;
+  static constexpr int kBoxCols = 128;
+  static constexpr int kColBoxes = 1;
+  static constexpr int kTileBytes = 1024;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr bool kPairRows = true;
 };
 
 template <typename T, int D>

@@ -1042,7 +1042,11 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
                 const int tj = t0 + kChunk * j;
                 const uint32_t kdst = stage + j * PS::kKV;
                 const uint32_t vdst = stage + (SUB + j) * PS::kKV;
-                if (!two) {
+                if constexpr (G::kPairRows) {  // rows of two tokens; blocks of >= 16 tokens (host-checked)
+                  const int y = (cur.kvh * p.block_size + (tj & (p.block_size - 1))) >> 1;
+                  tma_load_3d(kdst, &kmap, bar, 0, y, pbs0[j]);
+                  tma_load_3d(vdst, &vmap, bar, 0, y, pbs0[j]);
+                } else if (!two) {
                   const int y = cur.kvh * p.block_size + (tj & (p.block_size - 1));
 #pragma unroll
                   for (int cb = 0; cb < G::kColBoxes; ++cb) {

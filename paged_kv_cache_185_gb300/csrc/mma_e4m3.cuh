@@ -31,6 +31,16 @@
 
 namespace wllm {
 
+// Byte offset of 16-byte chunk `chunk` of token row `row` in a staged tile of
+// codes (two tokens per 128-byte row when head_dim is 64).
+template <int D>
+__device__ __forceinline__ uint32_t code_offset(int row, int chunk) {
+  if constexpr (Geom<uint8_t, D>::kPairRows)
+    return tile_offset(row >> 1, ((row & 1) << 2) | chunk);
+  else
+    return tile_offset(row, chunk);
+}
+
 // Query B fragments in the permuted head_dim order above, converted to f16
 // (exact for f16 queries; bf16 queries are rounded to f16).  Row stride D.
 template <typename T, int D, int NT>
@@ -97,7 +107,7 @@ __device__ __forceinline__ void mma_chunks_e4m3(MmaState<__half, D, NT>& st, uin
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
       uint32_t r[4];
-      ldsm_x4(k_base + j * kTile + tile_offset(a_row, 2 * kp + a_chunk), r);
+      ldsm_x4(k_base + j * kTile + code_offset<D>(a_row, 2 * kp + a_chunk), r);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         // token rows g (r[2 half]) and g + 8 (r[2 half + 1]): low pairs -> k 2c, 2c+1, high -> 2c+8, 2c+9
@@ -172,7 +182,7 @@ __device__ __forceinline__ void mma_chunks_e4m3(MmaState<__half, D, NT>& st, uin
 #pragma unroll
     for (int mp = 0; mp < D / 32; ++mp) {
       uint32_t r[4];  // tokens 0-7 / 8-15 of chunk 2mp, then of chunk 2mp + 1
-      ldsm_x4_trans(v_base + j * kTile + tile_offset(a_row, 2 * mp + a_chunk), r);
+      ldsm_x4_trans(v_base + j * kTile + code_offset<D>(a_row, 2 * mp + a_chunk), r);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         // bytes (t, e), (t, e+1), (t+1, e), (t+1, e+1) -> (t, e), (t+1, e), (t, e+1), (t+1, e+1)

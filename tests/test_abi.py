@@ -133,7 +133,7 @@ def good_fp8(B=2, Hq=4, Hkv=2, D=128, bs=16, nb=8, mb=4, dt=torch.bfloat16, q_st
 
 
 def test_fp8_decode_rejects_bad_arguments(lib):
-    assert decode_fp8(lib, **good_fp8(D=64)) == 2                              # head_dim 64
+    assert decode_fp8(lib, **good_fp8(D=64, bs=8), bs=8) == 2                  # head_dim 64 with 8-token blocks
     assert decode_fp8(lib, **good_fp8(dt=torch.float32)) == 1                  # fp32 queries
     a = good_fp8()
     a.update(kc=desc((8, 2, 16, 128), torch.bfloat16))

@@ -92,6 +92,8 @@ DECODE_CASES = [
     (64, 4, 128, 32, torch.bfloat16, [31, 32, 33, 2500, 777]),                          # GQA 16: two head tiles
     (8, 1, 128, 64, torch.float16, [1, 127, 128, 129, 6000]),                           # one kv head
     (16, 2, 256, 16, torch.float16, [4097, 12, 900]),
+    (32, 4, 64, 16, torch.float16, [1, 15, 16, 17, 700, 2048, 129]),                   # D 64 (two tokens a row)
+    (16, 16, 64, 32, torch.bfloat16, [33, 1000, 5, 64]),                                # D 64 MHA, bs 32
 ]
 
 
@@ -170,7 +172,7 @@ def test_fp8_decode_step_fused(dtype):
 
 
 def test_fp8_rejects_unsupported_shapes():
-    case = custom_case("fp8_d64", lens=[10], num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+    case = custom_case("fp8_d64", lens=[10], num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=8,
                        dtype=torch.float16, seed=1, append="none")
     kc, vc = fp8_pools(case)
     with pytest.raises(wllm.WllmError):
@@ -197,3 +199,22 @@ def test_fp8_full_size_llama2_7b_sampled():
                               rows=torch.from_numpy(rows), k_scale=K_SCALE, v_scale=V_SCALE)
     got = out.cpu().reshape(-1, case.head_dim)[torch.from_numpy(rows)]
     assert_attention_close(got, ref, case.dtype, "c2 fp8 sampled")
+
+
+def test_fp8_head_dim_64_step_with_shared_prefixes():
+    # TinyLlama-shaped heads (32/4, D 64) over an fp8 cache: the fused step, groups of 8 sharing 16 blocks
+    rng = np.random.default_rng(12)
+    lens = 256 + rng.integers(1, 1800, size=21)
+    case = custom_case("fp8_d64_step", lens=lens, num_q_heads=32, num_kv_heads=4, head_dim=64, block_size=16,
+                       dtype=torch.float16, seed=121, groups=(8, 16), append="tail")
+    kc, vc = fp8_pools(case)
+    kd, vd = kc.cuda(), vc.cuda()
+    q = case.q.cuda()
+    out = torch.empty_like(q)
+    wllm.decode_step_fp8(out, q, case.key.cuda(), case.value.cuda(), kd, vd, case.slot_mapping.cuda(),
+                         case.block_tables.cuda(), case.context_lens.cuda(), case.num_kv_heads, case.scale, 0.2, 0.3,
+                         case.block_size)
+    torch.cuda.synchronize()
+    oracle.reshape_and_cache_e4m3(case.key, case.value, kc, vc, case.slot_mapping, 0.2, 0.3)
+    assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc)
+    assert_attention_close(out.cpu(), oracle_decode_fp8(case, kc, vc, 0.2, 0.3), torch.float16, "fp8 D64 step")

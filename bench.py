@@ -558,7 +558,7 @@ def main():
     ap.add_argument("--graph-layers", type=int, default=8,
                     help="layers per CUDA-graph replay for the graph measurement (0: skip)")
     ap.add_argument("--fp8-reps", type=int, default=100,
-                    help="repetitions of the fp8-cache measurement (0: skip; head_dim 128/256 only)")
+                    help="repetitions of the fp8-cache measurement (0: skip)")
     ap.add_argument("--prefill-reps", type=int, default=50,
                     help="repetitions of the chunked-prefill measurement (0: skip)")
     ap.add_argument("--workload", default="c1", choices=list(workloads.CASE_NAMES))

@@ -102,6 +102,10 @@ def _load():
             vp, vp, i64, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
             ctypes.c_float, i32, i32]
         lib.oracle_paged_prefill_rows.restype = i32
+        lib.oracle_paged_prefill_rows_kv.argtypes = [
+            vp, vp, i64, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
+            ctypes.c_float, i32, i32, ctypes.c_float, ctypes.c_float, i32]
+        lib.oracle_paged_prefill_rows_kv.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -236,14 +240,16 @@ def paged_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
 
 def paged_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                   block_tables: torch.Tensor, context_lens: torch.Tensor, query_start_loc: torch.Tensor,
-                  num_kv_heads: int, scale: float, rows=None, num_threads: int = 0) -> torch.Tensor:
+                  num_kv_heads: int, scale: float, rows=None, num_threads: int = 0, k_scale: float = 1.0,
+                  v_scale: float = 1.0) -> torch.Tensor:
     """Chunked-prefill paged attention in float64.
 
     q [T,Hq,D] packed chunks (sequence b owns rows query_start_loc[b] ..
     query_start_loc[b+1]-1, the last n_b of its context_lens[b] tokens); caches
     [N_b,Hkv,bs,D] of q's dtype; block_tables int32 [B,M_b]; context_lens int32
-    [B]; query_start_loc int32 [B+1].  Returns float64 [T,Hq,D], or [len(rows),D]
-    for flat rows r = t*Hq + h.
+    [B]; query_start_loc int32 [B+1].  Caches may instead be uint8 E4M3 codes
+    whose values are code * k_scale (resp. v_scale).  Returns float64 [T,Hq,D],
+    or [len(rows),D] for flat rows r = t*Hq + h.
     """
     q = _host(q)
     kc, vc = _host(k_cache), _host(v_cache)
@@ -255,7 +261,8 @@ def paged_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     B = cl.shape[0]
     if Hkv != num_kv_heads or D2 != D or vc.shape != kc.shape or qsl.shape != (B + 1,):
         raise ValueError("shape mismatch")
-    if kc.dtype != q.dtype or vc.dtype != q.dtype:
+    fp8 = kc.dtype == torch.uint8
+    if vc.dtype != kc.dtype or not (fp8 or kc.dtype == q.dtype):
         raise ValueError("dtype mismatch")
     if bt.dim() != 2 or bt.shape[0] != B:
         raise ValueError("block_tables shape mismatch")
@@ -266,8 +273,10 @@ def paged_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         rows_t = torch.as_tensor(rows, dtype=torch.int64).contiguous()
         n_rows = rows_t.numel()
         out = torch.empty((n_rows, D), dtype=torch.float64)
-    _check(_load().oracle_paged_prefill_rows(
+    _check(_load().oracle_paged_prefill_rows_kv(
         out.data_ptr(), None if rows_t is None else rows_t.data_ptr(), n_rows,
         q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), cl.data_ptr(), qsl.data_ptr(),
-        B, T, Hq, Hkv, D, N_b, bs, bt.shape[1], float(scale), _DTYPE_CODE[q.dtype], int(num_threads)))
+        B, T, Hq, Hkv, D, N_b, bs, bt.shape[1], float(scale), _DTYPE_CODE[q.dtype],
+        E4M3 if fp8 else _DTYPE_CODE[q.dtype], float(k_scale) if fp8 else 1.0, float(v_scale) if fp8 else 1.0,
+        int(num_threads)))
     return out

@@ -370,17 +370,20 @@ int oracle_paged_decode_rows(double* out, const int64_t* rows, int64_t n_rows, c
  *   s_j = (double)scale * sum_d q[t][h][d] * K_j[d]   for j = 0 .. P,
  *   out[t][h][:] = sum_j exp(s_j - m) V_j[:] / sum_j exp(s_j - m),  m = max_j s_j.
  * rows: indices r = t * Hq + h (NULL: every row in order); out: binary64
- * [n_rows][D].  Decode is the case n_b = 1.  Inputs are validated first;
+ * [n_rows][D].  Decode is the case n_b = 1.  K/V are stored as kv_dtype
+ * (q's type, or E4M3 codes whose values are code * k_scale, resp.
+ * v_scale, the scales widened from binary32).  Inputs are validated first;
  * nothing is written on error.
  */
-int oracle_paged_prefill_rows(double* out, const int64_t* rows, int64_t n_rows, const void* q,
-                              const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                              const int32_t* context_lens, const int32_t* query_start_loc,
-                              int64_t num_seqs, int64_t num_tokens, int64_t num_q_heads,
-                              int64_t num_kv_heads, int64_t head_dim, int64_t num_blocks,
-                              int64_t block_size, int64_t max_blocks, float scale, int dtype,
-                              int num_threads) {
-  if (elt_bytes(dtype) == 0 || dtype == ORACLE_E4M3) return ORACLE_BAD_DTYPE;
+int oracle_paged_prefill_rows_kv(double* out, const int64_t* rows, int64_t n_rows, const void* q,
+                                 const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, const int32_t* query_start_loc,
+                                 int64_t num_seqs, int64_t num_tokens, int64_t num_q_heads,
+                                 int64_t num_kv_heads, int64_t head_dim, int64_t num_blocks,
+                                 int64_t block_size, int64_t max_blocks, float scale, int dtype,
+                                 int kv_dtype, float k_scale, float v_scale, int num_threads) {
+  if (elt_bytes(dtype) == 0 || dtype == ORACLE_E4M3 || elt_bytes(kv_dtype) == 0) return ORACLE_BAD_DTYPE;
+  const double ks = (double)k_scale, vs = (double)v_scale;
   if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || max_blocks < 0 || num_q_heads % num_kv_heads != 0)
     return ORACLE_BAD_SHAPE;
@@ -440,7 +443,8 @@ int oracle_paged_prefill_rows(double* out, const int64_t* rows, int64_t n_rows, 
       const int64_t pb = block_tables[b * max_blocks + j / block_size];
       const int64_t k_off = ((pb * num_kv_heads + c) * block_size + j % block_size) * head_dim;
       double dot = 0.0;
-      for (int64_t d = 0; d < head_dim; ++d) dot += load_elt(q, q_off + d, dtype) * load_elt(k_cache, k_off + d, dtype);
+      for (int64_t d = 0; d < head_dim; ++d)
+        dot += load_elt(q, q_off + d, dtype) * (load_elt(k_cache, k_off + d, kv_dtype) * ks);
       s[j] = scale_d * dot;
     }
     double m = s[0];
@@ -452,12 +456,26 @@ int oracle_paged_prefill_rows(double* out, const int64_t* rows, int64_t n_rows, 
       denom += w;
       const int64_t pb = block_tables[b * max_blocks + j / block_size];
       const int64_t v_off = ((pb * num_kv_heads + c) * block_size + j % block_size) * head_dim;
-      for (int64_t d = 0; d < head_dim; ++d) o[d] += w * load_elt(v_cache, v_off + d, dtype);
+      for (int64_t d = 0; d < head_dim; ++d) o[d] += w * (load_elt(v_cache, v_off + d, kv_dtype) * vs);
     }
     for (int64_t d = 0; d < head_dim; ++d) o[d] /= denom;
     free(s);
   }
   return status;
+}
+
+/* The same with K/V stored like q (scales 1). */
+int oracle_paged_prefill_rows(double* out, const int64_t* rows, int64_t n_rows, const void* q,
+                              const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                              const int32_t* context_lens, const int32_t* query_start_loc,
+                              int64_t num_seqs, int64_t num_tokens, int64_t num_q_heads,
+                              int64_t num_kv_heads, int64_t head_dim, int64_t num_blocks,
+                              int64_t block_size, int64_t max_blocks, float scale, int dtype,
+                              int num_threads) {
+  return oracle_paged_prefill_rows_kv(out, rows, n_rows, q, k_cache, v_cache, block_tables, context_lens,
+                                      query_start_loc, num_seqs, num_tokens, num_q_heads, num_kv_heads,
+                                      head_dim, num_blocks, block_size, max_blocks, scale, dtype, dtype,
+                                      1.0f, 1.0f, num_threads);
 }
 
 /* Number of threads an OpenMP region uses by default (1 without OpenMP). */

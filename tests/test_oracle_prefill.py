@@ -156,3 +156,22 @@ def test_prefill_rows_and_validation():
         oracle.paged_prefill(q, kp, vp, bt, torch.tensor([5, 12], dtype=torch.int32), qsl, 2, 0.125)
     with pytest.raises(oracle.OracleError):  # last start != T
         oracle.paged_prefill(q, kp, vp, bt, cl, torch.tensor([0, 10, 21], dtype=torch.int32), 2, 0.125)
+
+
+@pytest.mark.parametrize("qdtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (4, 4, 64)])
+def test_prefill_over_e4m3_codes_matches_dense_causal_sdpa(qdtype, Hq, Hkv, D):
+    lens, chunks = [40, 70, 5], [40, 22, 1]
+    gen = torch.Generator().manual_seed(Hq + D)
+    dk = [torch.randn(L, Hkv, D, generator=gen).to(torch.float8_e4m3fn) for L in lens]
+    dv = [torch.randn(L, Hkv, D, generator=gen).to(torch.float8_e4m3fn) for L in lens]
+    kp, vp, bt = paged_from_dense(dk, dv, 16, 12, gen, pad_blocks=1)
+    q = torch.randn(sum(chunks), Hq, D, generator=gen).to(qdtype)
+    qsl = torch.tensor(np.concatenate([[0], np.cumsum(chunks)]), dtype=torch.int32)
+    ks, vs, scale = 0.61, 1.7, float(np.float32(1 / math.sqrt(D)))
+    got = oracle.paged_prefill(q, kp.view(torch.uint8), vp.view(torch.uint8), bt, torch.tensor(lens, dtype=torch.int32),
+                               qsl, Hkv, scale, k_scale=ks, v_scale=vs)
+    k64 = [k.to(torch.float64) * float(np.float32(ks)) for k in dk]
+    v64 = [v.to(torch.float64) * float(np.float32(vs)) for v in dv]
+    ref = _dense_causal_sdpa(q, qsl, k64, v64, lens, scale)
+    torch.testing.assert_close(got, ref, rtol=1e-12, atol=1e-12)

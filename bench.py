@@ -199,6 +199,26 @@ def prefill_bench(args, case, dev, flush, stream):
         e[1].record(stream)
     torch.cuda.synchronize()
     ms = sum(e[0].elapsed_time(e[1]) for e in ev) / R
+    fp8_ms = None
+    if case.head_dim == 128 or case.block_size >= 16:  # the same chunks over E4M3 codes of the same K/V
+        k8 = (kc.float() * 4.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        v8 = (vc.float() * 4.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+        def call8():
+            wllm.paged_attention_prefill_fp8(out, q, k8, v8, bt, cl, qsl, case.num_kv_heads, case.scale, 0.25, 0.25,
+                                             case.block_size)
+
+        for _ in range(3):
+            flush.zero_()
+            call8()
+        ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+        for e in ev8:
+            flush.zero_()
+            e[0].record(stream)
+            call8()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        fp8_ms = sum(e[0].elapsed_time(e[1]) for e in ev8) / R
     flops = 0
     for p0 in prior:
         P = np.arange(int(p0), int(p0) + chunk)
@@ -215,6 +235,8 @@ def prefill_bench(args, case, dev, flush, stream):
             "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (mma.sync m16n8k16)",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_kind": kind, "flops": flops},
+            "fp8_cache_us": None if fp8_ms is None else fp8_ms * 1e3,
+            "fp8_cache_tflops": None if fp8_ms is None else flops / (fp8_ms / 1e3) / 1e12,
             "reps": R}
 
 

@@ -214,6 +214,21 @@ int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q,
                                  const wllm_tensor* query_start_loc, int num_kv_heads,
                                  float scale, int block_size, wllm_stream stream);
 
+/*
+ * Chunked prefill over E4M3 caches (the format of wllm_reshape_and_cache_fp8):
+ * the same call with K = code * k_scale and V = code * v_scale.  q/out rows
+ * 8-byte aligned; D 64 (block_size >= 16) or 128.  The codes are widened to
+ * f16 exactly on the device; bf16 queries are rounded to f16 for the
+ * products; accumulation is fp32.
+ */
+int wllm_paged_attention_prefill_fp8(const wllm_tensor* out, const wllm_tensor* q,
+                                     const wllm_tensor* k_cache, const wllm_tensor* v_cache,
+                                     const wllm_tensor* block_tables,
+                                     const wllm_tensor* context_lens,
+                                     const wllm_tensor* query_start_loc, int num_kv_heads,
+                                     float scale, float k_scale, float v_scale, int block_size,
+                                     wllm_stream stream);
+
 /* ---------------------------------------------------------------------------
  * FP8 (E4M3) KV cache.
  *

@@ -16,7 +16,7 @@ __all__ = ["reshape_and_cache", "paged_attention_decode", "paged_attention_decod
            "partition_tokens", "device_errors", "version", "load_library",
            "decode_step", "WllmError", "library_path", "BlockManager",
            "reshape_and_cache_fp8", "paged_attention_decode_fp8", "decode_step_fp8",
-           "paged_attention_prefill"]
+           "paged_attention_prefill", "paged_attention_prefill_fp8"]
 
 
 def __getattr__(name):

@@ -25,7 +25,7 @@ _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int32: 3,
 # every symbol include/wllm.h declares
 EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode", "wllm_decode_step",
             "wllm_reshape_and_cache_fp8", "wllm_paged_attention_decode_fp8", "wllm_decode_step_fp8",
-            "wllm_paged_attention_prefill",
+            "wllm_paged_attention_prefill", "wllm_paged_attention_prefill_fp8",
             "wllm_paged_attention_decode_noalloc",
             "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
             "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version",
@@ -85,6 +85,9 @@ def load_library():
         lib.wllm_paged_attention_prefill.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
                                                      ctypes.c_int, ctypes.c_void_p]
         lib.wllm_paged_attention_prefill.restype = ctypes.c_int
+        lib.wllm_paged_attention_prefill_fp8.argtypes = [P, P, P, P, P, P, P, ctypes.c_int, f32, f32, f32,
+                                                         ctypes.c_int, ctypes.c_void_p]
+        lib.wllm_paged_attention_prefill_fp8.restype = ctypes.c_int
         lib.wllm_paged_attention_decode_noalloc.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_float,
                                                             ctypes.c_int, ctypes.c_void_p]
         lib.wllm_paged_attention_decode_noalloc.restype = ctypes.c_int
@@ -252,6 +255,20 @@ def paged_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens
         args = [describe(x) for x in (out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc)]
         _check(lib.wllm_paged_attention_prefill(*[ctypes.byref(a) for a in args], int(num_kv_heads),
                                                 float(scale), int(block_size), _stream_handle(dev)))
+    return out
+
+
+def paged_attention_prefill_fp8(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                                num_kv_heads: int, scale: float, k_scale: float, v_scale: float,
+                                block_size: int) -> torch.Tensor:
+    """Chunked-prefill paged attention over E4M3 caches (K = code * k_scale, V = code * v_scale)."""
+    dev = _require_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        args = [describe(x) for x in (out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc)]
+        _check(lib.wllm_paged_attention_prefill_fp8(*[ctypes.byref(a) for a in args], int(num_kv_heads),
+                                                    float(scale), float(k_scale), float(v_scale),
+                                                    int(block_size), _stream_handle(dev)))
     return out
 
 

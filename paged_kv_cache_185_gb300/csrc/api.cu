@@ -925,10 +925,14 @@ int wllm_decode_step_fp8(const wllm_tensor* out, const wllm_tensor* q, const wll
 // ---------------------------------------------------------------------------
 // Chunked-prefill (multi-query) paged attention.
 // ---------------------------------------------------------------------------
-int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
-                                 const wllm_tensor* v_cache, const wllm_tensor* block_tables,
-                                 const wllm_tensor* context_lens, const wllm_tensor* query_start_loc,
-                                 int num_kv_heads, float scale, int block_size, wllm_stream stream) {
+}  // extern "C"
+
+namespace {
+
+int prefill_call(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                 const wllm_tensor* v_cache, const wllm_tensor* block_tables, const wllm_tensor* context_lens,
+                 const wllm_tensor* query_start_loc, int num_kv_heads, float scale, int block_size,
+                 wllm_stream stream, bool kv_fp8, float k_scale, float v_scale) {
   int rc;
   if ((rc = check_desc(out, "out", 3)) || (rc = check_desc(q, "q", 3)) ||
       (rc = check_desc(k_cache, "k_cache", 4)) || (rc = check_desc(v_cache, "v_cache", 4)) ||
@@ -937,8 +941,12 @@ int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, c
     return rc;
   const int dt = q->dtype;
   if (dt != WLLM_F16 && dt != WLLM_BF16) return fail(WLLM_ERR_UNSUPPORTED, "prefill takes F16 or BF16 inputs");
-  if (out->dtype != dt || k_cache->dtype != dt || v_cache->dtype != dt)
-    return fail(WLLM_ERR_INVALID_ARG, "q, out and caches must share one dtype");
+  const int kv_dt = kv_fp8 ? WLLM_FP8_E4M3 : dt;
+  if (out->dtype != dt) return fail(WLLM_ERR_INVALID_ARG, "out must have the dtype of q");
+  if (k_cache->dtype != kv_dt || v_cache->dtype != kv_dt)
+    return fail(WLLM_ERR_INVALID_ARG, kv_fp8 ? "caches must be FP8_E4M3" : "q, out and caches must share one dtype");
+  if (kv_fp8 && (!positive_finite(k_scale) || !positive_finite(v_scale)))
+    return fail(WLLM_ERR_INVALID_ARG, "k_scale and v_scale must be positive and finite");
   if (block_tables->dtype != WLLM_I32 || context_lens->dtype != WLLM_I32 || query_start_loc->dtype != WLLM_I32)
     return fail(WLLM_ERR_INVALID_ARG, "block_tables, context_lens and query_start_loc must be I32");
   if (!same_shape(out, q)) return fail(WLLM_ERR_INVALID_ARG, "out and q shapes differ");
@@ -966,6 +974,8 @@ int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, c
   if (d != 64 && d != 128) return fail(WLLM_ERR_UNSUPPORTED, "prefill head_dim %lld not supported (64, 128)", (long long)d);
   if (!is_pow2(bs) || bs < 8 || bs > 256)
     return fail(WLLM_ERR_UNSUPPORTED, "block_size %lld not supported (power of two in [8, 256])", (long long)bs);
+  if (kv_fp8 && d == 64 && bs < 16)
+    return fail(WLLM_ERR_UNSUPPORTED, "an fp8 cache with head_dim 64 needs block_size >= 16");
   if (T > INT32_MAX / 64 || B > INT32_MAX / 2 || hq > 65535 || hkv > 65535 || mb * bs > INT32_MAX || nb > INT32_MAX)
     return fail(WLLM_ERR_UNSUPPORTED, "sizes too large");
   if (T == 0 || B == 0 || hq == 0) return WLLM_OK;
@@ -975,14 +985,17 @@ int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, c
   if (!(aligned(q->data, 4) && aligned(out->data, 4) && q->stride[0] % 2 == 0 && q->stride[1] % 2 == 0 &&
         out->stride[0] % 2 == 0 && out->stride[1] % 2 == 0))
     return fail(WLLM_ERR_INVALID_ARG, "q/out rows must be 4-byte aligned");
+  if (kv_fp8 && !(aligned(q->data, 8) && aligned(out->data, 8) && q->stride[0] % 4 == 0 && q->stride[1] % 4 == 0 &&
+                  out->stride[0] % 4 == 0 && out->stride[1] % 4 == 0))
+    return fail(WLLM_ERR_INVALID_ARG, "prefill over an fp8 cache needs 8-byte aligned q/out rows");
 
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState* s = nullptr;
   if ((rc = device_state(&s))) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap kmap, vmap;
-  if ((rc = make_pool_map(&kmap, k_cache->data, dt, nb, hkv, bs, d, "k_cache"))) return rc;
-  if ((rc = make_pool_map(&vmap, v_cache->data, dt, nb, hkv, bs, d, "v_cache"))) return rc;
+  if ((rc = make_pool_map(&kmap, k_cache->data, kv_dt, nb, hkv, bs, d, "k_cache"))) return rc;
+  if ((rc = make_pool_map(&vmap, v_cache->data, kv_dt, nb, hkv, bs, d, "v_cache"))) return rc;
   const bool check = env_flag("WLLM_CHECK");
   if (check) {
     cudaError_t e = static_cast<cudaError_t>(launch_check_decode(
@@ -1012,14 +1025,38 @@ int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, c
   p.block_size = static_cast<int>(bs);
   p.log2_bs = ilog2(bs);
   p.num_blocks = static_cast<int>(nb);
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // an fp8 cache holds K / k_scale and V / v_scale: the scales return here
+  p.scale_log2 = (kv_fp8 ? scale * k_scale : scale) * 1.4426950408889634f;
+  p.v_scale = kv_fp8 ? v_scale : 1.f;
   p.err = s->err;
   p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
   const int grid_x = prefill_grid_x(T, B, p.group);
-  cudaError_t e = static_cast<cudaError_t>(launch_prefill(dt, static_cast<int>(d), kmap, vmap, p, grid_x, st));
+  cudaError_t e =
+      static_cast<cudaError_t>(launch_prefill(dt, static_cast<int>(d), kv_fp8, kmap, vmap, p, grid_x, st));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   if (check) return collect_device_errors(s, st, "paged_attention_prefill");
   return WLLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wllm_paged_attention_prefill(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                 const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                 const wllm_tensor* context_lens, const wllm_tensor* query_start_loc,
+                                 int num_kv_heads, float scale, int block_size, wllm_stream stream) {
+  return prefill_call(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_kv_heads, scale,
+                      block_size, stream, false, 1.f, 1.f);
+}
+
+int wllm_paged_attention_prefill_fp8(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
+                                     const wllm_tensor* v_cache, const wllm_tensor* block_tables,
+                                     const wllm_tensor* context_lens, const wllm_tensor* query_start_loc,
+                                     int num_kv_heads, float scale, float k_scale, float v_scale, int block_size,
+                                     wllm_stream stream) {
+  return prefill_call(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_kv_heads, scale,
+                      block_size, stream, true, k_scale, v_scale);
 }
 
 // ---------------------------------------------------------------------------

@@ -94,14 +94,16 @@ struct PrefillParams {
   const int32_t* query_start_loc;
   int num_seqs, num_tokens, num_q_heads, num_kv_heads, group;
   int max_blocks, block_size, log2_bs, num_blocks;
-  float scale_log2;               // scale * log2(e)
+  float scale_log2;               // scale * log2(e) (times k_scale for an fp8 cache)
+  float v_scale;                  // fp8 cache: factor of every output (1 otherwise)
   int* err;
   unsigned long long wait_limit_ns;
 };
 // CTAs along x for T packed tokens of B sequences (grid y = kv heads).
 int prefill_grid_x(int64_t num_tokens, int64_t num_seqs, int group);
-// f16/bf16 (dtype code 1/2), head_dim 64 or 128; returns a cudaError_t value.
-int launch_prefill(int dtype, int head_dim, const CUtensorMap& kmap, const CUtensorMap& vmap,
+// f16/bf16 queries (dtype code 1/2), head_dim 64 or 128; `kv_fp8`: E4M3 caches
+// (head_dim 64 needs blocks of >= 16 tokens).  Returns a cudaError_t value.
+int launch_prefill(int dtype, int head_dim, bool kv_fp8, const CUtensorMap& kmap, const CUtensorMap& vmap,
                    const PrefillParams& p, int grid_x, cudaStream_t stream);
 
 // Check-mode kernels: record index errors in the device error word.

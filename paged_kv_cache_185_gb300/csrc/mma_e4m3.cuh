@@ -31,6 +31,17 @@
 
 namespace wllm {
 
+// f16x2 of a pair of query elements (exact for f16; bf16 rounded to f16).
+template <typename T>
+__device__ __forceinline__ uint32_t to_f16x2(uint32_t pair) {
+  if constexpr (std::is_same<T, __half>::value) {
+    return pair;
+  } else {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pair));
+    return Mma<__half>::pack(f.x, f.y);
+  }
+}
+
 // Byte offset of 16-byte chunk `chunk` of token row `row` in a staged tile of
 // codes (two tokens per 128-byte row when head_dim is 64).
 template <int D>

@@ -19,9 +19,18 @@
 // softmax in the log2 domain, and O += P V with P taken straight from the S
 // accumulators.  CTAs are ordered so that the rows with the longest context
 // start first.  Every wait is bounded.
+//
+// Over an fp8 (E4M3) cache (F8) the stages hold codes (half the bytes) and the
+// products run in f16: K codes are widened in registers straight into B
+// fragments whose k order is a permutation of head_dim (the query's A
+// fragments take the same permutation), and V codes go through ldmatrix.trans
+// and a byte permute into B fragments of two interleaved head_dim tiles (even
+// and odd elements), re-interleaved at the output store; k_scale is folded into
+// the softmax scale and v_scale into the output.
 #include "common.cuh"
 #include "decode_kernel.cuh"
 #include "launch.h"
+#include "mma_e4m3.cuh"
 
 namespace wllm {
 
@@ -33,19 +42,21 @@ constexpr int kPfKv = 64;        // kv tokens per stage
 constexpr int kPfStep = 32;      // kv tokens per softmax step (a divisor of kPfKv; 64 measured slower)
 constexpr int kPfThreads = (kPfWarps + 1) * 32;
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 struct PfShape {
-  static constexpr int kSub = Geom<T, D>::kTileBytes;  // 16 rows of one head's K (or V)
+  using KT = typename std::conditional<F8, uint8_t, T>::type;  // cache element
+  static constexpr int kSub = Geom<KT, D>::kTileBytes;  // 16 rows of one head's K (or V)
   static constexpr int kStageBytes = 2 * (kPfKv / 16) * kSub;
   static constexpr int kStages = (96 * 1024) / kStageBytes;  // two CTAs per SM
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 2 * kStages * 8 + 64;
 };
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(kPfThreads, 2)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                          const PrefillParams p) {
-  using PS = PfShape<T, D>;
+  using PS = PfShape<T, D, F8>;
+  using MT = typename std::conditional<F8, __half, T>::type;  // tensor-core operand type
   constexpr int S = PS::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -157,7 +168,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         break;
       }
       if (lane == 0) {
-        using G16 = Geom<T, D>;
+        using G16 = Geom<typename PS::KT, D>;
         const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
         const uint32_t bar = smem_u32(full + s);
         uint32_t bytes = 0;
@@ -173,7 +184,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           if (t >= kv_end) continue;
           const uint32_t kdst = stage + j * PS::kSub;
           const uint32_t vdst = stage + (4 + j) * PS::kSub;
-          if (!two) {
+          if constexpr (G16::kPairRows) {  // rows of two tokens; blocks of >= 16 tokens (host-checked)
+            const int y = (kvh * p.block_size + (t & (p.block_size - 1))) >> 1;
+            tma_load_3d(kdst, &kmap, bar, 0, y, ent0[j]);
+            tma_load_3d(vdst, &vmap, bar, 0, y, ent0[j]);
+          } else if (!two) {
             const int y = kvh * p.block_size + (t & (p.block_size - 1));
 #pragma unroll
             for (int cb = 0; cb < G16::kColBoxes; ++cb) {
@@ -224,11 +239,22 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                       static_cast<int64_t>(kvh * G + (vb ? rb % G : 0)) * p.q_sh;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      const int d = ks * 16 + 2 * c;
-      qa[ks][0] = va ? *reinterpret_cast<const uint32_t*>(qrow_a + d) : 0u;
-      qa[ks][1] = vb ? *reinterpret_cast<const uint32_t*>(qrow_b + d) : 0u;
-      qa[ks][2] = va ? *reinterpret_cast<const uint32_t*>(qrow_a + d + 8) : 0u;
-      qa[ks][3] = vb ? *reinterpret_cast<const uint32_t*>(qrow_b + d + 8) : 0u;
+      if constexpr (F8) {
+        // k 2c, 2c+1 <-> d 16ks+4c, +1 and k 2c+8, 2c+9 <-> d 16ks+4c+2, +3 (the K codes' order)
+        const int d = ks * 16 + 4 * c;
+        const uint2 za = va ? *reinterpret_cast<const uint2*>(qrow_a + d) : make_uint2(0u, 0u);
+        const uint2 zb = vb ? *reinterpret_cast<const uint2*>(qrow_b + d) : make_uint2(0u, 0u);
+        qa[ks][0] = to_f16x2<T>(za.x);
+        qa[ks][1] = to_f16x2<T>(zb.x);
+        qa[ks][2] = to_f16x2<T>(za.y);
+        qa[ks][3] = to_f16x2<T>(zb.y);
+      } else {
+        const int d = ks * 16 + 2 * c;
+        qa[ks][0] = va ? *reinterpret_cast<const uint32_t*>(qrow_a + d) : 0u;
+        qa[ks][1] = vb ? *reinterpret_cast<const uint32_t*>(qrow_b + d) : 0u;
+        qa[ks][2] = va ? *reinterpret_cast<const uint32_t*>(qrow_a + d + 8) : 0u;
+        qa[ks][3] = vb ? *reinterpret_cast<const uint32_t*>(qrow_b + d + 8) : 0u;
+      }
     }
   }
   float o[D / 8][4];
@@ -266,15 +292,34 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         for (int nt = 0; nt < NN; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+        if constexpr (F8) {
+          // one ldmatrix: tokens 0-7 / 8-15 of the sub-tile x code chunks 2kp, 2kp+1 (k steps 2kp, 2kp+1)
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
+          for (int kp = 0; kp < D / 32; ++kp) {
 #pragma unroll
-          for (int j = 0; j < NJ; ++j) {
-            uint32_t r[4];
-            ldsm_x4(kt + (NJ * h + j) * PS::kSub + tile_offset(kb_row, 2 * ks + kb_chunk), r);
-            const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
-            Mma<T>::run(sc[2 * j], qa[ks], b0);
-            Mma<T>::run(sc[2 * j + 1], qa[ks], b1);
+            for (int j = 0; j < NJ; ++j) {
+              uint32_t r[4];
+              ldsm_x4(kt + (NJ * h + j) * PS::kSub + code_offset<D>(kb_row, 2 * kp + kb_chunk), r);
+              uint32_t b[4][2];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(r[i], b[i][0], b[i][1]);
+              Mma<__half>::run(sc[2 * j], qa[2 * kp], b[0]);
+              Mma<__half>::run(sc[2 * j], qa[2 * kp + 1], b[1]);
+              Mma<__half>::run(sc[2 * j + 1], qa[2 * kp], b[2]);
+              Mma<__half>::run(sc[2 * j + 1], qa[2 * kp + 1], b[3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+              uint32_t r[4];
+              ldsm_x4(kt + (NJ * h + j) * PS::kSub + tile_offset(kb_row, 2 * ks + kb_chunk), r);
+              const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
+              Mma<T>::run(sc[2 * j], qa[ks], b0);
+              Mma<T>::run(sc[2 * j + 1], qa[ks], b1);
+            }
           }
         }
         // causal mask where the step reaches past a row's position (and past kv_end)
@@ -313,8 +358,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           const float p2 = exp2f(sc[nt][2] - mn_b), p3 = exp2f(sc[nt][3] - mn_b);
           sum_a += p0 + p1;
           sum_b += p2 + p3;
-          pa_frag[nt >> 1][(nt & 1) * 2 + 0] = Mma<T>::pack(p0, p1);
-          pa_frag[nt >> 1][(nt & 1) * 2 + 1] = Mma<T>::pack(p2, p3);
+          pa_frag[nt >> 1][(nt & 1) * 2 + 0] = Mma<MT>::pack(p0, p1);
+          pa_frag[nt >> 1][(nt & 1) * 2 + 1] = Mma<MT>::pack(p2, p3);
         }
         l_a = l_a * al_a + sum_a;
         l_b = l_b * al_b + sum_b;
@@ -337,13 +382,36 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             keep0 = (tk < kv_end ? 0x0000ffffu : 0u) | (tk + 1 < kv_end ? 0xffff0000u : 0u);
             keep1 = (tk + 8 < kv_end ? 0x0000ffffu : 0u) | (tk + 9 < kv_end ? 0xffff0000u : 0u);
           }
+          if constexpr (F8) {
+            // tokens 0-7 / 8-15 x code chunks 2dq, 2dq+1; per chunk m two output tiles:
+            // o[2m] holds d = 16m + 2g (even elements), o[2m+1] d = 16m + 2g + 1
 #pragma unroll
-          for (int dp = 0; dp < D / 16; ++dp) {
-            uint32_t r[4];
-            ldsm_x4_trans(vt + (NJ * h + j) * PS::kSub + tile_offset(vb_row, 2 * dp + vb_chunk), r);
-            const uint32_t b0[2] = {r[0] & keep0, r[1] & keep1}, b1[2] = {r[2] & keep0, r[3] & keep1};
-            Mma<T>::run(o[2 * dp], pa_frag[j], b0);
-            Mma<T>::run(o[2 * dp + 1], pa_frag[j], b1);
+            for (int dq = 0; dq < D / 32; ++dq) {
+              uint32_t r[4];
+              ldsm_x4_trans(vt + (NJ * h + j) * PS::kSub + code_offset<D>(vb_row, 2 * dq + vb_chunk), r);
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                uint32_t ev[2], od[2];  // [tokens 0-7, tokens 8-15]
+                e4m3x4_to_f16x2x2(__byte_perm(r[2 * half], 0u, 0x3120), ev[0], od[0]);
+                e4m3x4_to_f16x2x2(__byte_perm(r[2 * half + 1], 0u, 0x3120), ev[1], od[1]);
+                ev[0] &= keep0;
+                od[0] &= keep0;
+                ev[1] &= keep1;
+                od[1] &= keep1;
+                const int m = 2 * dq + half;
+                Mma<__half>::run(o[2 * m], pa_frag[j], ev);
+                Mma<__half>::run(o[2 * m + 1], pa_frag[j], od);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+              uint32_t r[4];
+              ldsm_x4_trans(vt + (NJ * h + j) * PS::kSub + tile_offset(vb_row, 2 * dp + vb_chunk), r);
+              const uint32_t b0[2] = {r[0] & keep0, r[1] & keep1}, b1[2] = {r[2] & keep0, r[3] & keep1};
+              Mma<T>::run(o[2 * dp], pa_frag[j], b0);
+              Mma<T>::run(o[2 * dp + 1], pa_frag[j], b1);
+            }
           }
         }
       }
@@ -358,27 +426,37 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   l_b += __shfl_xor_sync(kFullMask, l_b, 1);
   l_b += __shfl_xor_sync(kFullMask, l_b, 2);
   T* out = reinterpret_cast<T*>(p.out);
-  if (va) {
-    const float inv = 1.f / l_a;
-    T* orow = out + static_cast<int64_t>(s0 + ra / G) * p.o_st + static_cast<int64_t>(kvh * G + ra % G) * p.o_sh;
 #pragma unroll
-    for (int dt = 0; dt < D / 8; ++dt)
-      *reinterpret_cast<uint32_t*>(orow + dt * 8 + 2 * c) = Mma<T>::pack(o[dt][0] * inv, o[dt][1] * inv);
-  }
-  if (vb) {
-    const float inv = 1.f / l_b;
-    T* orow = out + static_cast<int64_t>(s0 + rb / G) * p.o_st + static_cast<int64_t>(kvh * G + rb % G) * p.o_sh;
+  for (int rr = 0; rr < 2; ++rr) {  // row a (accumulator entries 0, 1), then row b (2, 3)
+    const bool valid = rr == 0 ? va : vb;
+    if (!valid) continue;
+    const int row = rr == 0 ? ra : rb;
+    const float inv = (F8 ? p.v_scale : 1.f) / (rr == 0 ? l_a : l_b);
+    T* orow = out + static_cast<int64_t>(s0 + row / G) * p.o_st + static_cast<int64_t>(kvh * G + row % G) * p.o_sh;
+    if constexpr (F8) {
+      // chunk m: d = 16m + 4c + {0, 1, 2, 3} = even tile entry 0, odd 0, even 1, odd 1
 #pragma unroll
-    for (int dt = 0; dt < D / 8; ++dt)
-      *reinterpret_cast<uint32_t*>(orow + dt * 8 + 2 * c) = Mma<T>::pack(o[dt][2] * inv, o[dt][3] * inv);
+      for (int m = 0; m < D / 16; ++m) {
+        const float* ev = o[2 * m];
+        const float* od = o[2 * m + 1];
+        *reinterpret_cast<uint2*>(orow + 16 * m + 4 * c) =
+            make_uint2(Mma<T>::pack(ev[2 * rr] * inv, od[2 * rr] * inv),
+                       Mma<T>::pack(ev[2 * rr + 1] * inv, od[2 * rr + 1] * inv));
+      }
+    } else {
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt)
+        *reinterpret_cast<uint32_t*>(orow + dt * 8 + 2 * c) =
+            Mma<T>::pack(o[dt][2 * rr] * inv, o[dt][2 * rr + 1] * inv);
+    }
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 int launch_prefill_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const PrefillParams& p, int grid_x,
                         cudaStream_t stream) {
-  using PS = PfShape<T, D>;
-  auto kernel = paged_prefill_kernel<T, D>;
+  using PS = PfShape<T, D, F8>;
+  auto kernel = paged_prefill_kernel<T, D, F8>;
   static int configured_for[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -392,6 +470,22 @@ int launch_prefill_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
   return cudaGetLastError();
 }
 
+template <bool F8>
+int launch_prefill_f(int dtype, int head_dim, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     const PrefillParams& p, int grid_x, cudaStream_t stream) {
+  const bool bf16 = dtype == 2;  // wllm_dtype codes: 1 f16, 2 bf16
+  switch (head_dim) {
+    case 64:
+      return bf16 ? launch_prefill_inst<__nv_bfloat16, 64, F8>(kmap, vmap, p, grid_x, stream)
+                  : launch_prefill_inst<__half, 64, F8>(kmap, vmap, p, grid_x, stream);
+    case 128:
+      return bf16 ? launch_prefill_inst<__nv_bfloat16, 128, F8>(kmap, vmap, p, grid_x, stream)
+                  : launch_prefill_inst<__half, 128, F8>(kmap, vmap, p, grid_x, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
 int prefill_grid_x(int64_t num_tokens, int64_t num_seqs, int group) {
@@ -399,20 +493,11 @@ int prefill_grid_x(int64_t num_tokens, int64_t num_seqs, int group) {
   return static_cast<int>((num_tokens * group + kPfRows - 1) / kPfRows + num_seqs);
 }
 
-int launch_prefill(int dtype, int head_dim, const CUtensorMap& kmap, const CUtensorMap& vmap,
+int launch_prefill(int dtype, int head_dim, bool kv_fp8, const CUtensorMap& kmap, const CUtensorMap& vmap,
                    const PrefillParams& p, int grid_x, cudaStream_t stream) {
   if (grid_x <= 0) return cudaSuccess;
-  const bool bf16 = dtype == 2;  // wllm_dtype codes: 1 f16, 2 bf16
-  switch (head_dim) {
-    case 64:
-      return bf16 ? launch_prefill_inst<__nv_bfloat16, 64>(kmap, vmap, p, grid_x, stream)
-                  : launch_prefill_inst<__half, 64>(kmap, vmap, p, grid_x, stream);
-    case 128:
-      return bf16 ? launch_prefill_inst<__nv_bfloat16, 128>(kmap, vmap, p, grid_x, stream)
-                  : launch_prefill_inst<__half, 128>(kmap, vmap, p, grid_x, stream);
-    default:
-      return cudaErrorInvalidValue;
-  }
+  return kv_fp8 ? launch_prefill_f<true>(dtype, head_dim, kmap, vmap, p, grid_x, stream)
+                : launch_prefill_f<false>(dtype, head_dim, kmap, vmap, p, grid_x, stream);
 }
 
 }  // namespace wllm

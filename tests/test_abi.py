@@ -200,3 +200,27 @@ def test_prefill_rejects_bad_arguments(lib):
     a.update(q=desc((10, 4, 64), torch.bfloat16, stride=(257, 64, 1)))  # rows not 4-byte aligned
     assert prefill(lib, **a) == 1
     assert prefill(lib, **good_prefill(T=0)) == 0                       # nothing to do
+
+
+def test_prefill_fp8_rejects_bad_arguments(lib):
+    r = lambda x: None if x is None else ctypes.byref(x)  # noqa: E731
+
+    def call(a, ks=0.5, vs=0.5, bs=16, hkv=2):
+        return lib.wllm_paged_attention_prefill_fp8(r(a["out"]), r(a["q"]), r(a["kc"]), r(a["vc"]), r(a["bt"]),
+                                                    r(a["cl"]), r(a["qsl"]), hkv, 0.125, ks, vs, bs, None)
+
+    def good8(**kw):
+        a = good_prefill(**kw)
+        D, bs = kw.get("D", 64), kw.get("bs", 16)
+        a.update(kc=desc((8, 2, bs, D), torch.uint8), vc=desc((8, 2, bs, D), torch.uint8))
+        return a
+
+    assert call(good8(D=64, bs=8), bs=8) == 2                      # head_dim 64 with 8-token blocks
+    assert call(good8(D=256)) == 2                                 # head_dim 256
+    assert call(good_prefill()) == 1                               # 16-bit caches
+    assert call(good8(), ks=0.0) == 1
+    assert call(good8(), vs=float("nan")) == 1
+    a = good8()
+    a.update(q=desc((10, 4, 64), torch.bfloat16, stride=(258, 64, 1)))  # rows 4- but not 8-byte aligned
+    assert call(a) == 1
+    assert call(good8(T=0)) == 0

@@ -122,3 +122,49 @@ def test_prefill_reports_inconsistent_query_starts(monkeypatch):
         wllm.paged_attention_prefill(out, q.to(dev), kc, vc, case.block_tables.to(dev), cl.to(dev), bad.to(dev), 2,
                                      case.scale, 16)
     assert wllm.device_errors() == 0  # the failing call cleared the word
+
+
+FP8_CASES = [c for c in CASES if not (c[2] == 64 and c[3] < 16)]  # D 64 needs blocks of >= 16 tokens
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs,lens,chunks", FP8_CASES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_prefill_fp8_matches_oracle(Hq, Hkv, D, bs, lens, chunks, dtype):
+    from paged_kv_cache_185_gb300.workloads import e4m3_codes
+    case, q, qsl = prefill_case(lens, chunks, Hq, Hkv, D, bs, dtype, seed=Hq * 5 + D + bs)
+    kc, vc = case.pool("cpu")
+    k8, v8 = e4m3_codes(kc, 4.0), e4m3_codes(vc, 4.0)
+    dev = "cuda"
+    out = torch.empty(q.shape, dtype=dtype, device=dev)
+    wllm.paged_attention_prefill_fp8(out, q.to(dev), k8.to(dev), v8.to(dev), case.block_tables.to(dev),
+                                     case.context_lens.to(dev), qsl.to(dev), Hkv, case.scale, 0.25, 0.3, bs)
+    torch.cuda.synchronize()
+    ref = oracle.paged_prefill(q, k8, v8, case.block_tables, case.context_lens, qsl, Hkv, case.scale,
+                               k_scale=0.25, v_scale=0.3)
+    assert_attention_close(out.cpu(), ref, dtype, f"fp8 prefill {Hq}/{Hkv} D{D} bs{bs}")
+
+
+def test_prefill_fp8_long_chunks_sampled_and_refusals():
+    from paged_kv_cache_185_gb300.workloads import e4m3_codes
+    rng = np.random.default_rng(6)
+    prior = rng.integers(0, 2500, size=3)
+    lens = [int(p) + 700 for p in prior]
+    case, q, qsl = prefill_case(lens, [700] * 3, 28, 4, 128, 16, torch.bfloat16, seed=61)
+    kc, vc = case.pool("cpu")
+    k8, v8 = e4m3_codes(kc, 4.0), e4m3_codes(vc, 4.0)
+    dev = "cuda"
+    out = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    wllm.paged_attention_prefill_fp8(out, q.to(dev), k8.to(dev), v8.to(dev), case.block_tables.to(dev),
+                                     case.context_lens.to(dev), qsl.to(dev), 4, case.scale, 0.25, 0.25, 16)
+    torch.cuda.synchronize()
+    rows = np.sort(rng.choice(q.shape[0] * 28, size=200, replace=False))
+    ref = oracle.paged_prefill(q, k8, v8, case.block_tables, case.context_lens, qsl, 4, case.scale,
+                               rows=torch.from_numpy(rows), k_scale=0.25, v_scale=0.25)
+    assert_attention_close(out.cpu().reshape(-1, 128)[torch.from_numpy(rows)], ref, torch.bfloat16, "fp8 long")
+    # head_dim 64 with 8-token blocks is refused on the host
+    c8, q8, qsl8 = prefill_case([40], [40], 4, 2, 64, 8, torch.float16, seed=62)
+    k8, v8 = e4m3_codes(c8.pool("cpu")[0], 4.0), e4m3_codes(c8.pool("cpu")[1], 4.0)
+    with pytest.raises(wllm.WllmError):
+        wllm.paged_attention_prefill_fp8(torch.empty(q8.shape, dtype=q8.dtype, device=dev), q8.to(dev), k8.to(dev),
+                                         v8.to(dev), c8.block_tables.to(dev), c8.context_lens.to(dev),
+                                         qsl8.to(dev), 2, c8.scale, 1.0, 1.0, 8)

@@ -149,3 +149,15 @@ def test_large_workload_tables(name):
         bt = c.block_tables
         for g in range(0, 256, 8):
             assert (bt[g:g + 8, :64] == bt[g, :64]).all()
+
+
+def test_e4m3_codes_draws_torch_codes_and_keeps_nan():
+    from paged_kv_cache_185_gb300.workloads import e4m3_codes
+    x = torch.tensor([[1.0, -2.5, float("nan")], [0.001, 100.0, -0.0]])
+    got = e4m3_codes(x, 2.0)
+    ref = (x.float() * 2.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert got.dtype == torch.uint8 and got.shape == x.shape
+    assert torch.equal(got, ref)
+    assert got[0, 2] & 0x7F == 0x7F
+    with pytest.raises(ValueError):
+        e4m3_codes(torch.tensor([300.0]), 2.0)  # 600 is outside E4M3

@@ -331,14 +331,33 @@ def _c4(r=0):
                        num_blocks=n_b, append="tail", heavy_key_frac=0.01, heavy_key_factor=8.0)
 
 
-_BUILDERS = {"c0": _c0, "c1": _c1, "c2": _c2, "c3": _c3, "c4": _c4}
+# Report-only rows: a Gemma-shaped multi-query geometry (one kv head, head_dim
+# 256) and the Llama-2-shaped batch over 32-token blocks.
+def _gemma_mqa(r=0):
+    rng = np.random.default_rng(1005 + 100000 * r)
+    lens = rng.integers(1024, 4096, size=128, endpoint=True)
+    return custom_case("gemma_mqa_decode", lens=lens, num_q_heads=8, num_kv_heads=1, head_dim=256,
+                       block_size=16, dtype=torch.bfloat16, seed=1005 + 100000 * r, append="tail")
+
+
+def _bs32(r=0):
+    rng = np.random.default_rng(1006 + 100000 * r)
+    lens = rng.integers(1024, 4096, size=128, endpoint=True)
+    return custom_case("llama2_7b_bs32_decode", lens=lens, num_q_heads=32, num_kv_heads=32, head_dim=128,
+                       block_size=32, dtype=torch.bfloat16, seed=1006 + 100000 * r, spare_blocks=32,
+                       append="free", n_append=128)
+
+
+_BUILDERS = {"c0": _c0, "c1": _c1, "c2": _c2, "c3": _c3, "c4": _c4, "gemma_mqa": _gemma_mqa, "bs32": _bs32}
 CASE_NAMES = tuple(_BUILDERS)
 
 
 def make_case(name: str, replica: int = 0) -> DecodeCase:
-    """One of the five workloads: c0 (tiny, fp32), c1 (TinyLlama-1.1B-shaped),
+    """One of the workloads: c0 (tiny, fp32), c1 (TinyLlama-1.1B-shaped),
     c2 (Llama-2-7B-shaped MHA), c3 (Qwen2.5-7B-shaped GQA with shared prefixes),
-    c4 (long-context, 32K-128K tokens, ~120 GB pool).  ``replica`` > 0 draws an
+    c4 (long-context, 32K-128K tokens, ~120 GB pool), and the report-only rows
+    gemma_mqa (8/1 heads, head_dim 256) and bs32 (c2's shape over 32-token
+    blocks).  ``replica`` > 0 draws an
     independent batch of the same recipe (another seed)."""
     return _BUILDERS[name](replica)
 

@@ -48,7 +48,7 @@ def test_tiny_workload_matches_oracle_and_golden():
     assert_attention_close(got, gold, case.dtype, "c0 golden")
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "gemma_mqa", "bs32"])
 def test_workload_matches_oracle(name):
     case = workloads.make_case(name)
     got, kc, vc = gpu_step(case)

@@ -232,9 +232,9 @@ int wllm_paged_attention_prefill_fp8(const wllm_tensor* out, const wllm_tensor* 
 /* ---------------------------------------------------------------------------
  * FP8 (E4M3) KV cache.
  *
- * Passage: "wLLM" project page, "Features / Core engine" (the paged KV cache
- * and its decode kernel; storing the cache in fewer bytes is the lever on a
- * step that reads the whole cache).  The storage format is this library's
+ * Passage: "vLLM on Windows" build README, release table ("KV compression"
+ * column: fp8 listed as a KV-cache dtype of every release).  The page names
+ * no format; the storage format is this library's
  * reading: each cache element is the E4M3 code of the element divided by a
  * per-tensor scale (one k_scale for every K element, one v_scale for every V
  * element, binary32, positive and finite):
@@ -291,23 +291,27 @@ int wllm_decode_step_fp8(const wllm_tensor* out, const wllm_tensor* q, const wll
 /*
  * Paged decode attention that allocates no device memory.
  *
- * There is no counterpart to this call in the pages; it exists for callers
- * that cannot let a library allocate: one that is capturing a CUDA graph
- * (cudaMalloc is not permitted inside a capture), an engine whose memory
- * manager has already reserved all device memory for its own KV pool and
- * activations, or a latency-critical caller that cannot accept the implicit
- * device synchronisation of cudaMalloc/cudaFree.  It computes the same result
- * with the same kernels as wllm_paged_attention_decode and takes the same
+ * There is no counterpart to this call in the pages.  It is for callers that
+ * cannot let a library allocate device memory: an engine whose memory manager
+ * has already reserved all device memory for its own KV pool and activations
+ * (a cudaMalloc there fails, or takes memory the manager counts on), or a
+ * latency-critical caller that cannot accept the implicit device
+ * synchronisation of cudaMalloc/cudaFree.  It computes the same result with
+ * the same kernel as wllm_paged_attention_decode and takes the same
  * arguments; the caller still owns and passes every input and output.
  *
  * Scratch: the split-KV partial results and the kernel's error and scheduler
  * words live in one fixed 32 MiB array inside the library's device image,
  * which every GPU that loads the library holds until the process exits.
  *   - The first call on a device looks that array's device address up (once,
- *     with the device current); make that first call before any stream
- *     capture.
- *   - Each call clears the words that must start at zero (a stream-ordered
- *     memset of 256 bytes); the partials keep the last call's contents.
+ *     with the device current).  Make that first call before any stream
+ *     capture: made while its stream is capturing, it returns
+ *     WLLM_ERR_INVALID_ARG and launches nothing.
+ *   - Each call clears the scheduler words, which must start at zero (a
+ *     stream-ordered memset of 192 bytes); the partials keep the last call's
+ *     contents, and the error word keeps its bits until wllm_device_errors()
+ *     reads and clears it (it reports this call's errors together with the
+ *     other calls').
  *   - All calls on a device share the array: calls that overlap on the GPU
  *     (different streams, not ordered) race and give wrong results.
  * Supported: F16/BF16 inputs, query rows 16-byte aligned (the persistent
@@ -315,7 +319,9 @@ int wllm_decode_step_fp8(const wllm_tensor* out, const wllm_tensor* q, const wll
  * whose partial results would not fit in the array (many long sequences cut
  * into many partitions) return WLLM_ERR_UNSUPPORTED with the byte counts in
  * wllm_last_error(); nothing is launched then.  Check mode is not available
- * here.
+ * here: a block-table entry outside [0, N_b) or a length above M_b*bs is
+ * clamped on the device, as in wllm_paged_attention_decode, and recorded in
+ * the error word for wllm_device_errors().
  */
 int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tensor* q,
                                         const wllm_tensor* k_cache, const wllm_tensor* v_cache,
@@ -325,7 +331,8 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
 
 /*
  * Bytes of device workspace that wllm_paged_attention_decode needs for these
- * sizes (0 when no sequence is split).  The workspace holds the split-KV
+ * sizes (0 when no sequence is split).  num_kv_heads is an argument because
+ * the merge counters are kept per (sequence, kv head, head tile).  The workspace holds the split-KV
  * partial results and two counters per (sequence, kv head, head tile) for the
  * merge inside the launch.  Every launch leaves the counters at zero; after a
  * launch reports a timed-out wait (error bit 4), wllm_device_errors() zeroes
@@ -356,12 +363,34 @@ int wllm_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads, int h
                           int max_blocks_per_seq, int block_size, int dtype);
 
 /*
- * Read and clear the device error word of the current device: bit 0 slot out
- * of range, bit 1 block id out of range, bit 2 context length out of range,
- * bit 3 duplicate slot (check mode), bit 4 a bounded wait on a copy timed out.
+ * Read and clear the device error words of the current device (the one of
+ * the regular calls and the one of wllm_paged_attention_decode_noalloc, OR-ed
+ * together): bit 0 slot out of range, bit 1 block id out of range, bit 2
+ * context length out of range, bit 3 duplicate slot (check mode), bit 4 a
+ * bounded wait timed out.  Clearing also puts the scheduler and merge counters
+ * back to zero, which a launch that gave up on a wait may have left set.
  * Synchronises the device.  Returns -1 if it could not be read.
  */
 int wllm_device_errors(void);
+
+/*
+ * Self-test of the bounded waits (no counterpart in the pages; it tests this
+ * library's failure reporting).  Launches a one-thread kernel that waits on an
+ * mbarrier that never receives its arrival and then polls a device counter
+ * that never reaches its target, each with the same bounded waits the decode
+ * kernels use, limited to limit_ns (in (0, 1e9], else WLLM_ERR_INVALID_ARG).
+ * Both waits give up: the kernel sets bit 4 of the device error word and
+ * leaves the persistent scheduler's claim counter non-zero, as a decode that
+ * gave up half-way would.  The call synchronises `stream` and returns WLLM_OK
+ * when both waits reported their timeout.  Call wllm_device_errors() next: it
+ * returns bit 4 and puts the counters back to zero; decode calls made before
+ * that are wrong.
+ */
+int wllm_selftest_wait_timeout(unsigned long long limit_ns, wllm_stream stream);
+
+/* Kernel launches the library has issued in this process (a running count;
+ * the difference over a region counts that region's launches). */
+unsigned long long wllm_launch_count(void);
 
 /* Thread-local message for the last call that did not return WLLM_OK. */
 const char* wllm_last_error(void);

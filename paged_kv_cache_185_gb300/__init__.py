@@ -13,7 +13,8 @@ from __future__ import annotations
 
 __all__ = ["reshape_and_cache", "paged_attention_decode", "paged_attention_decode_noalloc",
            "workspace_bytes", "set_workspace",
-           "partition_tokens", "device_errors", "version", "load_library",
+           "partition_tokens", "device_errors", "selftest_wait_timeout", "launch_count", "version",
+           "load_library",
            "decode_step", "WllmError", "library_path", "BlockManager",
            "reshape_and_cache_fp8", "paged_attention_decode_fp8", "decode_step_fp8",
            "paged_attention_prefill", "paged_attention_prefill_fp8"]

@@ -28,7 +28,8 @@ EXPORTED = ("wllm_reshape_and_cache", "wllm_paged_attention_decode", "wllm_decod
             "wllm_paged_attention_prefill", "wllm_paged_attention_prefill_fp8",
             "wllm_paged_attention_decode_noalloc",
             "wllm_paged_attention_workspace_bytes", "wllm_set_workspace",
-            "wllm_partition_tokens", "wllm_device_errors", "wllm_last_error", "wllm_version",
+            "wllm_partition_tokens", "wllm_device_errors", "wllm_selftest_wait_timeout", "wllm_launch_count",
+            "wllm_last_error", "wllm_version",
             "wllm_bm_create", "wllm_bm_destroy", "wllm_bm_add_sequence", "wllm_bm_append_token",
             "wllm_bm_fork", "wllm_bm_free_sequence", "wllm_bm_block_table", "wllm_bm_num_free_blocks",
             "wllm_bm_num_cached_blocks", "wllm_bm_block_ref")
@@ -99,6 +100,10 @@ def load_library():
         lib.wllm_partition_tokens.restype = ctypes.c_int
         lib.wllm_device_errors.argtypes = []
         lib.wllm_device_errors.restype = ctypes.c_int
+        lib.wllm_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+        lib.wllm_selftest_wait_timeout.restype = ctypes.c_int
+        lib.wllm_launch_count.argtypes = []
+        lib.wllm_launch_count.restype = ctypes.c_ulonglong
         lib.wllm_last_error.argtypes = []
         lib.wllm_last_error.restype = ctypes.c_char_p
         lib.wllm_version.argtypes = []
@@ -295,6 +300,20 @@ def partition_tokens(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_p
 
 def device_errors() -> int:
     return int(load_library().wllm_device_errors())
+
+
+def selftest_wait_timeout(limit_ns: int, device=None) -> None:
+    """Run the bounded-wait self-test kernel on the current stream (see
+    wllm_selftest_wait_timeout); call device_errors() afterwards."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        _check(lib.wllm_selftest_wait_timeout(int(limit_ns), _stream_handle(dev)))
+
+
+def launch_count() -> int:
+    """Kernel launches the library has issued in this process."""
+    return int(load_library().wllm_launch_count())
 
 
 def version() -> str:

@@ -82,7 +82,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         raise RuntimeError("nvcc failed")
     tmp = LIB + f".{os.getpid()}.tmp"
     link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for _, o, _ in results],
-            "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
+            "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc), "-Xlinker", "-z,defs"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -98,6 +99,12 @@ int decode_smem_bytes(int dtype, int head_dim, DecodeVariant v, int head_tile) {
   }
 }
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int decode_threads(int dtype, int head_dim) {
   switch (dtype) {
     case WLLM_BF16: return threads_decode_bf16(head_dim);
@@ -164,9 +171,9 @@ int device_state(DeviceState** out) {
   if (!s.ready) {
     e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = cudaMalloc(reinterpret_cast<void**>(&s.err), 256);
+    e = cudaMalloc(reinterpret_cast<void**>(&s.err), kCtrlBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
-    e = cudaMemset(s.err, 0, 256);
+    e = cudaMemset(s.err, 0, kCtrlBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
     s.ready = true;
   }
@@ -182,7 +189,7 @@ int collect_device_errors(DeviceState* s, cudaStream_t stream, const char* op) {
   e = cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
   if (word != 0) {
-    cudaMemset(s->err, 0, 256);
+    cudaMemset(s->err, 0, kCtrlBytes);
     return fail(WLLM_ERR_OUT_OF_RANGE, "%s: device index check failed (error bits 0x%x)", op, word);
   }
   return WLLM_OK;
@@ -409,7 +416,9 @@ extern "C" {
 
 const char* wllm_last_error(void) { return g_last_error.c_str(); }
 
-const char* wllm_version(void) { return "wllm-gb300 0.1.0 (sm_103a)"; }
+const char* wllm_version(void) { return "wllm-gb300 0.2.0 (sm_103a)"; }
+
+unsigned long long wllm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
 
@@ -510,6 +519,10 @@ extern "C" {
 }  // extern "C"
 
 namespace {
+
+// The allocation-free decode's error word on the current device (defined
+// with that call, below).
+int noalloc_take_errors();
 
 // The append after its argument checks.
 int run_append(AppendParams& ap, wllm_stream stream) {
@@ -615,9 +628,32 @@ int wllm_device_errors(void) {
   // clearing also resets the persistent kernel's scheduler words, which an
   // aborted launch may have left non-zero, and after a timed-out wait (bit 4)
   // the merge counters
-  if (word != 0 && cudaMemset(s->err, 0, 256) != cudaSuccess) return -1;
+  if (word != 0 && cudaMemset(s->err, 0, kCtrlBytes) != cudaSuccess) return -1;
   if ((word & 16) && s->counter_bytes > 0 && cudaMemset(s->ws, 0, s->counter_bytes) != cudaSuccess) return -1;
-  return word;
+  const int noalloc = noalloc_take_errors();
+  if (noalloc < 0) return -1;
+  return word | noalloc;
+}
+
+int wllm_selftest_wait_timeout(unsigned long long limit_ns, wllm_stream stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ULL)
+    return fail(WLLM_ERR_INVALID_ARG, "limit_ns must be in (0, 1e9]");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc) return rc;
+  int* result = nullptr;  // which waits gave up, kept in the control block's spare words
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  result = s->err + kSelftestResultOffset;
+  cudaError_t e = static_cast<cudaError_t>(
+      launch_wait_selftest(s->err, kSelftestNeverOffset, kSchedNextOffset, limit_ns, result, st));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  int r = 0;
+  e = cudaMemcpyAsync(&r, result, sizeof r, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test result");
+  if (r != 3) return fail(WLLM_ERR_CUDA, "self-test: waits that gave up 0x%x, expected both (0x3)", r);
+  return WLLM_OK;
 }
 
 namespace {
@@ -1062,20 +1098,21 @@ int wllm_paged_attention_prefill_fp8(const wllm_tensor* out, const wllm_tensor* 
 // ---------------------------------------------------------------------------
 // Allocation-free decode.
 //
-// Some callers cannot let a library allocate device memory: a caller that is
-// capturing a CUDA graph (cudaMalloc is not allowed inside a capture), an
-// engine whose memory manager has reserved all device memory for its own KV
-// pool and activations, or a latency-critical caller that cannot accept the
-// implicit device synchronisation of cudaMalloc/cudaFree.  For them this
+// Some callers cannot let a library allocate device memory: an engine whose
+// memory manager has reserved all device memory for its own KV pool and
+// activations, or a latency-critical caller that cannot accept the implicit
+// device synchronisation of cudaMalloc/cudaFree.  For them this
 // entry point takes its split-KV scratch (the per-partition partial results)
 // and its scheduler/error words from a fixed array in the library's device
 // image, sized kNoAllocScratchBytes.  Every GPU that loads the library holds
 // that array until the process exits.
 // ---------------------------------------------------------------------------
+}  // extern "C"
+
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
-constexpr size_t kNoAllocControlBytes = 256;                // error + scheduler words
+constexpr size_t kNoAllocControlBytes = kCtrlBytes;         // error + scheduler words
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -1084,14 +1121,22 @@ uint8_t* g_noalloc_addr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device.  The host-side
 // symbol is only a stand-in; the real address comes from the runtime, once per
-// device, with that device current.
-int noalloc_scratch(uint8_t** out) {
+// device, with that device current.  That lookup is refused while `stream` is
+// being captured into a graph.
+int noalloc_scratch(uint8_t** out, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(WLLM_ERR_UNSUPPORTED, "device index %d too large", dev);
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (g_noalloc_addr[dev] == nullptr) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(WLLM_ERR_INVALID_ARG,
+                  "the first allocation-free decode on a device looks up its scratch array and must not be made "
+                  "while the stream is being captured");
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
@@ -1101,7 +1146,27 @@ int noalloc_scratch(uint8_t** out) {
   return WLLM_OK;
 }
 
+// Read and clear the allocation-free decode's error word on the current device
+// (0 when that call has not been used there); the caller has synchronised the
+// device.  Clearing also resets its scheduler words.  -1 on a CUDA error.
+int noalloc_take_errors() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  uint8_t* ctrl = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    ctrl = g_noalloc_addr[dev];
+  }
+  if (ctrl == nullptr) return 0;
+  int word = 0;
+  if (cudaMemcpy(&word, ctrl, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (word != 0 && cudaMemset(ctrl, 0, kNoAllocControlBytes) != cudaSuccess) return -1;
+  return word;
+}
+
 }  // namespace
+
+extern "C" {
 
 int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor* k_cache,
                                         const wllm_tensor* v_cache, const wllm_tensor* block_tables,
@@ -1160,9 +1225,9 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
   int num_sms = 0;
   e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  uint8_t* scratch = nullptr;
-  if ((rc = noalloc_scratch(&scratch))) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch, st))) return rc;
 
   // plan every slice first: reject before launching anything
   for (int64_t b0 = 0; b0 < B; b0 += kPersistentMaxSeqs) {
@@ -1185,9 +1250,12 @@ int wllm_paged_attention_decode_noalloc(const wllm_tensor* out, const wllm_tenso
   for (int64_t b0 = 0; b0 < B; b0 += kPersistentMaxSeqs) {
     const int64_t nbat = std::min<int64_t>(kPersistentMaxSeqs, B - b0);
     const DecodePlan pl = make_plan(dt, nbat, hq, hkv, d, mb, bs, true, num_sms);
-    // the error and scheduler words must start at zero; partials need no clearing
-    e = cudaMemsetAsync(scratch, 0, kNoAllocControlBytes, st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(control words)");
+    // the scheduler words must start at zero; the error word (the first
+    // 64 bytes) keeps its bits until wllm_device_errors() reads it; partials
+    // need no clearing
+    e = cudaMemsetAsync(scratch + kSchedNextOffset * sizeof(int), 0,
+                        kNoAllocControlBytes - kSchedNextOffset * sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scheduler words)");
     DecodeParams p{};
     p.out = static_cast<uint8_t*>(out->data) + b0 * out->stride[0] * elt;
     p.q = static_cast<const uint8_t*>(q->data) + b0 * q->stride[0] * elt;

@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Poll a counter in global memory (acquire loads) until it reaches `target`,
+// giving up after `limit_ns`.  Returns false on timeout.
+__device__ __forceinline__ bool counter_wait_bounded(const int* ctr, int target, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    int c;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(c) : "l"(ctr) : "memory");
+    if (c >= target) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(128);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 3-D tiled bulk tensor copy global -> shared, completion on an mbarrier
 // ---------------------------------------------------------------------------

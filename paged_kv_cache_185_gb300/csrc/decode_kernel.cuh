@@ -668,18 +668,15 @@ int launch_decode_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const D
                        cudaStream_t stream) {
   using KS = KernelShape<T, D, NT, kMma>;
   auto kernel = paged_decode_kernel<T, D, NT, kMma>;
-  static int configured_for[64] = {0};  // per device: shared-memory attribute set
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<int> configured_for[64];  // per device: shared-memory attribute set
+  cudaError_t e = static_cast<cudaError_t>(
+      raise_smem_limit(configured_for, reinterpret_cast<const void*>(kernel), KS::kSmemBytes));
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured_for[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KS::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_for[dev] = 1;
-  }
   dim3 grid(p.num_seqs, p.max_parts, p.num_kv_heads * p.num_head_tiles);
   kernel<<<grid, KS::kWarps * 32, KS::kSmemBytes, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 template <typename T, int D, int NT, bool kMma>

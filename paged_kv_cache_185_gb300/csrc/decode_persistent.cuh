@@ -46,12 +46,6 @@
 
 namespace wllm {
 
-// the scheduler and grid-barrier words live next to the error word (offsets in ints)
-constexpr int kSchedNextOffset = 16;
-constexpr int kSchedDoneOffset = 32;
-constexpr int kGridCountOffset = 48;
-constexpr int kGridGenOffset = 56;
-
 // fused-step flags of one launch
 enum : int { kFuseAppend = 1, kOverlapCombine = 2 };
 
@@ -1466,20 +1460,18 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
   using PS = PShape<T, D, NT, F8>;
   auto kernel = paged_decode_persistent<T, D, NT, F8>;
   const int smem = persistent_smem<T, D, NT, F8>(p.num_seqs);
-  static int configured_for[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<int> configured_for[64];
+  cudaError_t e = static_cast<cudaError_t>(
+      raise_smem_limit(configured_for, reinterpret_cast<const void*>(kernel), 227 * 1024));
   if (e != cudaSuccess) return e;
-  if (dev < 64 && configured_for[dev] < smem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_for[dev] = 227 * 1024;
-  }
   AppendParams none{};
   const AppendParams& app = ap != nullptr ? *ap : none;
   const int flags = (ap != nullptr ? kFuseAppend : 0) | (fuse_combine ? kOverlapCombine : 0);
   if (flags == 0) {
     kernel<<<grid, PS::kThreads, smem, stream>>>(kmap, vmap, p, app, flags);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    note_launch();
   } else {
     // cooperative (every CTA resident), through the extensible launch so that
     // stream capture records it as a cooperative kernel node
@@ -1495,24 +1487,41 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, p, app, flags);
     if (e != cudaSuccess) return e;
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    note_launch();
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess || !separate_combine || fuse_combine) return e;
+  if (!separate_combine || fuse_combine) return cudaSuccess;
   splitkv_combine<T, D><<<(p.num_seqs * p.num_q_heads + 7) / 8, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 template <typename T, int D, int NT, bool F8 = false>
 int persistent_occupancy(int num_seqs) {
-  int blocks = 0;
+  // the answer depends only on the shared-memory size: the last one asked per
+  // device is remembered as (smem << 8 | blocks)
+  static std::atomic<long long> last[64];
   const int smem = persistent_smem<T, D, NT, F8>(num_seqs);
-  if (cudaFuncSetAttribute(paged_decode_persistent<T, D, NT, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           227 * 1024) != cudaSuccess)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const bool tracked = dev >= 0 && dev < 64;
+  if (tracked) {
+    const long long v = last[dev].load(std::memory_order_relaxed);
+    if (v != 0 && (v >> 8) == smem) return static_cast<int>(v & 255);
+  }
+  static std::atomic<int> configured_for[64];
+  if (raise_smem_limit(configured_for, reinterpret_cast<const void*>(paged_decode_persistent<T, D, NT, F8>),
+                       227 * 1024) != cudaSuccess)
     return 1;
+  int blocks = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, paged_decode_persistent<T, D, NT, F8>,
                                                     PShape<T, D, NT, F8>::kThreads, smem) != cudaSuccess)
     return 1;
-  return blocks < 1 ? 1 : blocks;
+  blocks = blocks < 1 ? 1 : (blocks > 255 ? 255 : blocks);
+  if (tracked) last[dev].store((static_cast<long long>(smem) << 8) | blocks, std::memory_order_relaxed);
+  return blocks;
 }
 
 }  // namespace wllm

@@ -6,7 +6,40 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace wllm {
+
+// The 256-byte per-device control block, offsets in ints: the error word;
+// two spare words used only by the bounded-wait self-test (a counter that
+// stays zero, and its result); the persistent scheduler's claim and finish
+// counters; the fused step's grid-barrier count and generation.
+constexpr int kCtrlBytes = 256;
+constexpr int kSelftestNeverOffset = 8;
+constexpr int kSelftestResultOffset = 9;
+constexpr int kSchedNextOffset = 16;
+constexpr int kSchedDoneOffset = 32;
+constexpr int kGridCountOffset = 48;
+constexpr int kGridGenOffset = 56;
+
+// Kernel launches the library has issued (successful launch calls), for
+// wllm_launch_count().  Every launch site calls note_launch() once per kernel.
+void note_launch();
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: `configured` is the kernel's own per-device record
+// (64 entries).  Thread-safe; two threads racing only repeat the attribute call.
+inline int raise_smem_limit(std::atomic<int>* configured, const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < 64;
+  if (tracked && configured[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (tracked) configured[dev].store(bytes, std::memory_order_release);
+  return cudaSuccess;
+}
 
 // Everything one paged-decode launch needs besides the two tensor maps.
 struct DecodeParams {
@@ -79,6 +112,13 @@ constexpr int kPersistentMaxSeqs = 1024;      // sequences per launch (the host 
 constexpr int kPersistentMaxParts = 256;      // partitions per sequence (the host widens partitions to fit)
 
 int launch_append(const AppendParams& p, cudaStream_t stream);
+
+// One-thread kernel whose two bounded waits (an mbarrier and the counter at
+// ctrl[never_offset], which must stay below 1) time out after limit_ns: sets
+// kErrWaitTimeout in ctrl[0], adds 1 to ctrl[sched_offset] and writes which
+// waits gave up (bit 0 mbarrier, bit 1 counter) to *result (device memory).
+int launch_wait_selftest(int* ctrl, int never_offset, int sched_offset, unsigned long long limit_ns, int* result,
+                         cudaStream_t stream);
 
 // Chunked-prefill (multi-query) paged attention: q/out [T][Hq][D] packed by
 // sequence (query_start_loc [B+1]); each chunk is the last n_b of the

@@ -457,17 +457,14 @@ int launch_prefill_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const 
                         cudaStream_t stream) {
   using PS = PfShape<T, D, F8>;
   auto kernel = paged_prefill_kernel<T, D, F8>;
-  static int configured_for[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<int> configured_for[64];
+  cudaError_t e = static_cast<cudaError_t>(
+      raise_smem_limit(configured_for, reinterpret_cast<const void*>(kernel), PS::kSmem));
   if (e != cudaSuccess) return e;
-  if (dev < 64 && configured_for[dev] < PS::kSmem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PS::kSmem);
-    if (e != cudaSuccess) return e;
-    configured_for[dev] = PS::kSmem;
-  }
   kernel<<<dim3(grid_x, p.num_kv_heads), kPfThreads, PS::kSmem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 template <bool F8>

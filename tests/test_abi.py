@@ -38,6 +38,36 @@ def test_library_exports_every_declared_symbol(lib):
     assert "sm_103a" in binding.version()
 
 
+def test_library_exports_nothing_else_with_c_linkage(lib):
+    """Unmangled dynamic symbols of the library are exactly the header's calls."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True)
+    names = {ln.split()[-1] for ln in out.stdout.splitlines() if ln.strip()}
+    plain = {n for n in names if not n.startswith("_Z") and not n.startswith("_")}
+    assert plain == set(declared_functions()), plain ^ set(declared_functions())
+
+
+def test_selftest_rejects_bad_limits_on_the_host(lib):
+    for limit in (0, 2_000_000_000):
+        assert lib.wllm_selftest_wait_timeout(limit, None) == binding.WLLM_ERR_INVALID_ARG
+        assert b"limit_ns" in lib.wllm_last_error()
+
+
+def test_launch_count_unchanged_by_rejected_calls(lib):
+    n0 = lib.wllm_launch_count()
+    q = desc([2, 4, 64], torch.float16)
+    kc = desc([8, 2, 16, 64], torch.float16)
+    bt = desc([2, 4], torch.int32)
+    cl = desc([2], torch.int32)
+    out = desc([2, 4, 64], torch.float32)  # wrong dtype: rejected on the host
+    assert decode(lib, out, q, kc, kc, bt, cl) == binding.WLLM_ERR_INVALID_ARG
+    assert lib.wllm_launch_count() == n0
+
+
 def desc(shape, dtype, data=FAKE, stride=None):
     d = binding.WllmTensor()
     d.data = data

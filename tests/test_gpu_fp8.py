@@ -218,3 +218,52 @@ def test_fp8_head_dim_64_step_with_shared_prefixes():
     oracle.reshape_and_cache_e4m3(case.key, case.value, kc, vc, case.slot_mapping, 0.2, 0.3)
     assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc)
     assert_attention_close(out.cpu(), oracle_decode_fp8(case, kc, vc, 0.2, 0.3), torch.float16, "fp8 D64 step")
+
+
+# --------------------------------------------------------------------------
+# the Qwen2.5-shaped prefix batch and the long-context batch at full size,
+# through the fused step the benchmark times
+# --------------------------------------------------------------------------
+
+def _fp8_fused_full_size(name, rows=None):
+    """decode_step_fp8 over E4M3 codes of the workload's referenced blocks (the
+    compact pool: the same tokens and sharing, renumbered), against the
+    oracle's E4M3 append and its attention over the dequantised codes."""
+    case = make_case(name)
+    kc, vc, bt, slots = case.compact()
+    kc, vc = e4m3_codes(kc, AMP), e4m3_codes(vc, AMP)
+    kd, vd = kc.cuda(), vc.cuda()
+    q = case.q.cuda()
+    out = torch.full_like(q, float("nan"))
+    wllm.decode_step_fp8(out, q, case.key.cuda(), case.value.cuda(), kd, vd, slots.cuda(), bt.cuda(),
+                         case.context_lens.cuda(), case.num_kv_heads, case.scale, K_SCALE, V_SCALE, case.block_size)
+    torch.cuda.synchronize()
+    oracle.reshape_and_cache_e4m3(case.key, case.value, kc, vc, slots, K_SCALE, V_SCALE)
+    assert torch.equal(kd.cpu(), kc) and torch.equal(vd.cpu(), vc), "E4M3 append not bit-exact"
+    del kd, vd
+    ref = oracle.paged_decode(case.q, kc, vc, bt, case.context_lens, case.num_kv_heads, case.scale,
+                              rows=rows, k_scale=K_SCALE, v_scale=V_SCALE)
+    got = out.cpu()
+    assert torch.isfinite(got).all(), "every row written"
+    if rows is not None:
+        got = got.reshape(-1, case.head_dim)[rows]
+    return got, ref, case
+
+
+def test_fp8_full_size_qwen25_prefix_step():
+    """256 sequences in groups of 8 sharing a 1024-token prompt: prefix-group
+    units over E4M3 codes, every row."""
+    got, ref, case = _fp8_fused_full_size("c3")
+    assert_attention_close(got, ref, case.dtype, "c3 fp8 fused step")
+
+
+def test_fp8_full_size_long_context_step_sampled():
+    """32K-128K tokens per sequence, up to 128 partitions merged per sequence,
+    1% keys x8: sampled rows."""
+    case = make_case("c4")
+    B, Hq = case.num_seqs, case.num_q_heads
+    g = torch.Generator().manual_seed(45)
+    rows = torch.tensor(sorted(set(torch.randint(0, B * Hq, (40,), generator=g).tolist()) |
+                               {b * Hq + (b * 7 + 2) % Hq for b in range(B)}))
+    got, ref, case = _fp8_fused_full_size("c4", rows=rows)
+    assert_attention_close(got, ref, case.dtype, "c4 fp8 fused step, sampled rows")

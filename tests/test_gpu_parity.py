@@ -83,6 +83,38 @@ def test_long_context_workload_sampled():
     assert_attention_close(flat, ref, case.dtype, "c4 sampled rows")
 
 
+def test_long_context_fused_step_sampled():
+    """The long-context batch through the fused step (append, grid barrier,
+    decode, in-launch merge of up to 128 partitions per sequence) over the full
+    ~120 GB pool, as the benchmark times it: sampled rows against the oracle
+    (which reads only the referenced blocks), the append bit for bit."""
+    case = workloads.make_case("c4")
+    free = torch.cuda.mem_get_info()[0]
+    need = 2 * case.pool_bytes() + (4 << 30)
+    assert free > need, f"needs {need / 2**30:.0f} GiB of device memory, {free / 2**30:.0f} free"
+    kc, vc = case.pool("cuda")
+    q = case.q.cuda()
+    out = torch.full_like(q, float("nan"))
+    wllm.decode_step(out, q, case.key.cuda(), case.value.cuda(), kc, vc, case.slot_mapping.cuda(),
+                     case.block_tables.cuda(), case.context_lens.cuda(), case.num_kv_heads, case.scale,
+                     case.block_size)
+    torch.cuda.synchronize()
+    ids = case.used_blocks.cuda()
+    k_used, v_used = kc[ids].cpu(), vc[ids].cpu()
+    del kc, vc
+    torch.cuda.empty_cache()
+    B, Hq = case.num_seqs, case.num_q_heads
+    g = torch.Generator().manual_seed(44)
+    rows = sorted(set(torch.randint(0, B * Hq, (40,), generator=g).tolist()) |
+                  {b * Hq + (b * 3 + 1) % Hq for b in range(B)})
+    ref, kr, vr = oracle_step(case, rows=rows, compact=True)
+    assert torch.equal(int_view(k_used), int_view(kr))
+    assert torch.equal(int_view(v_used), int_view(vr))
+    got = out.cpu()
+    assert torch.isfinite(got).all(), "every row written"
+    assert_attention_close(got.reshape(B * Hq, -1)[rows], ref, case.dtype, "c4 fused step, sampled rows")
+
+
 # ---------------------------------------------------------------------------
 # shape sweep: dtype x head_dim x block_size x GQA group, ragged lengths
 # ---------------------------------------------------------------------------

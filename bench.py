@@ -635,7 +635,8 @@ def run_ours(args):
                             cpu_budget=(3.0 if small else 2.0) if with_cpu else 0.0,
                             single_budget=2.0 if (with_cpu and small) else 0.0,
                             fp8_reps=min(args.fp8_reps, sub_steps))
-    graph = graph_layers(args, args.graph_workload, rank, dev, flush, stream) if args.graph_workload else None
+    graph = (graph_layers(args, args.graph_workload, rank, dev, flush, stream)
+             if args.graph_workload not in ("", "none") else None)
     prefill = {}
     for name in ([] if args.prefill_workloads in ("", "none") else args.prefill_workloads.split(",")):
         prefill[name] = prefill_bench(args, name, dev, flush, stream)
@@ -673,7 +674,7 @@ def main():
     ap.add_argument("--sub-steps", type=int, default=500, help="timed steps of each per-workload record")
     ap.add_argument("--pool", default="full", choices=["full", "compact"],
                     help="compact: only the referenced blocks on the device (the same bytes read; for ncu)")
-    ap.add_argument("--graph-workload", default="c1", help="workload of the CUDA-graph measurement ('' skips)")
+    ap.add_argument("--graph-workload", default="c1", help="workload of the CUDA-graph measurement ('none' skips)")
     ap.add_argument("--graph-layers", type=int, default=8,
                     help="layers per CUDA-graph replay for the graph measurement (0: skip)")
     ap.add_argument("--fp8-reps", type=int, default=100,

@@ -25,7 +25,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwllm.so")
 
 SOURCES = ["api.cu", "append.cu", "decode_bf16.cu", "decode_f16.cu", "decode_f32.cu", "decode_f8_f16.cu",
-           "decode_f8_bf16.cu", "prefill.cu", "block_manager.cpp"]
+           "decode_f8_bf16.cu", "prefill.cu", "prefill_tc.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

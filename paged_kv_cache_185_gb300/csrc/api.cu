@@ -1066,9 +1066,19 @@ int prefill_call(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor
   p.v_scale = kv_fp8 ? v_scale : 1.f;
   p.err = s->err;
   p.wait_limit_ns = static_cast<unsigned long long>(env_int("WLLM_WAIT_LIMIT_NS", 200000000LL));
-  const int grid_x = prefill_grid_x(T, B, p.group);
-  cudaError_t e =
-      static_cast<cudaError_t>(launch_prefill(dt, static_cast<int>(d), kv_fp8, kmap, vmap, p, grid_x, st));
+  // the tcgen05 kernel for 16-bit caches with 16-byte aligned q/out rows;
+  // WLLM_PREFILL_KERNEL=mma selects the mma.sync kernel
+  const bool rows16 = aligned(q->data, 16) && aligned(out->data, 16) && q->stride[0] % 8 == 0 &&
+                      q->stride[1] % 8 == 0 && out->stride[0] % 8 == 0 && out->stride[1] % 8 == 0;
+  const bool use_tc = !kv_fp8 && rows16 && !env_is("WLLM_PREFILL_KERNEL", "mma");
+  cudaError_t e;
+  if (use_tc) {
+    const int grid_x = prefill_tc_grid_x(T, B, p.group);
+    e = static_cast<cudaError_t>(launch_prefill_tc(dt, static_cast<int>(d), kmap, vmap, p, grid_x, st));
+  } else {
+    const int grid_x = prefill_grid_x(T, B, p.group);
+    e = static_cast<cudaError_t>(launch_prefill(dt, static_cast<int>(d), kv_fp8, kmap, vmap, p, grid_x, st));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   if (check) return collect_device_errors(s, st, "paged_attention_prefill");
   return WLLM_OK;

@@ -1,7 +1,9 @@
 """Chunked-prefill paged attention on the GPU, through the C ABI, against the
 oracle: packed query chunks (fresh prompts, continued prompts, one-token and
 empty chunks), GQA/MHA, head dims 64/128, block sizes 8..64, and a large
-sampled case."""
+sampled case.  16-bit caches run on the tcgen05 kernel when the q/out rows are
+16-byte aligned; the mma.sync kernel (WLLM_PREFILL_KERNEL=mma, misaligned rows,
+fp8 caches) is covered by the same cases."""
 import math
 
 import numpy as np
@@ -16,10 +18,10 @@ from tests.gpu_common import assert_attention_close
 pytestmark = pytest.mark.gpu
 
 
-def prefill_case(lens, chunks, Hq, Hkv, D, bs, dtype, seed):
+def prefill_case(lens, chunks, Hq, Hkv, D, bs, dtype, seed, **kw):
     """Pools holding every sequence's L tokens (the chunk's K/V appended) and packed query chunks."""
     case = custom_case("prefill", lens=lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
-                       dtype=dtype, seed=seed, spare_blocks=2, append="none")
+                       dtype=dtype, seed=seed, spare_blocks=2, append="none", **kw)
     gen = torch.Generator().manual_seed(seed + 7)
     T = int(sum(chunks))
     q = torch.randn(T, Hq, D, generator=gen).to(dtype)
@@ -55,16 +57,23 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=["tcgen05", "mma"])
+def kernel(request, monkeypatch):
+    if request.param == "mma":
+        monkeypatch.setenv("WLLM_PREFILL_KERNEL", "mma")
+    return request.param
+
+
 @pytest.mark.parametrize("Hq,Hkv,D,bs,lens,chunks", CASES)
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-def test_prefill_matches_oracle(Hq, Hkv, D, bs, lens, chunks, dtype):
+def test_prefill_matches_oracle(Hq, Hkv, D, bs, lens, chunks, dtype, kernel):
     case, q, qsl = prefill_case(lens, chunks, Hq, Hkv, D, bs, dtype, seed=Hq * 3 + D + bs)
     got = run_gpu(case, q, qsl)
     ref = run_oracle(case, q, qsl)
     assert_attention_close(got, ref, dtype, f"prefill {Hq}/{Hkv} D{D} bs{bs}")
 
 
-def test_prefill_one_token_chunks_match_decode():
+def test_prefill_one_token_chunks_match_decode(kernel):
     # n_b = 1 everywhere: the decode's answer
     rng = np.random.default_rng(2)
     lens = rng.integers(1, 3000, size=20)
@@ -80,7 +89,7 @@ def test_prefill_one_token_chunks_match_decode():
     assert_attention_close(dec.cpu(), ref, torch.bfloat16, "decode")
 
 
-def test_prefill_strided_output_and_query():
+def test_prefill_strided_output_and_query(kernel):
     # q and out as slices of wider buffers (a fused QKV projection and a padded output)
     case, q, qsl = prefill_case([90, 40], [90, 15], 8, 2, 64, 16, torch.float16, seed=31)
     dev = "cuda"
@@ -95,7 +104,33 @@ def test_prefill_strided_output_and_query():
     assert (wide_o[:, 0] == 7).all() and (wide_o[:, 9] == 7).all()
 
 
-def test_prefill_long_chunks_sampled():
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_prefill_heavy_keys_move_the_running_max(dtype, kernel):
+    """3% of the keys scaled x8: scores jump by far more than 2^8 in the log2
+    domain deep into the context, so the running maximum moves mid-row and O
+    is rescaled (in TMEM, for the tcgen05 kernel)."""
+    case, q, qsl = prefill_case([1500, 900, 2100], [300, 900, 64], 28, 4, 128, 16, dtype, seed=71,
+                                heavy_key_frac=0.03, heavy_key_factor=8.0)
+    got = run_gpu(case, q, qsl)
+    assert_attention_close(got, run_oracle(case, q, qsl), dtype, f"heavy keys {kernel}")
+
+
+def test_prefill_misaligned_rows_use_the_mma_kernel():
+    """q rows only 4-byte aligned: the call still succeeds (mma.sync kernel)."""
+    case, q, qsl = prefill_case([70, 200], [70, 33], 8, 2, 64, 16, torch.float16, seed=72)
+    dev = "cuda"
+    buf = torch.zeros(q.numel() + 2, dtype=q.dtype, device=dev)
+    qd = buf[2:].view(q.shape)
+    qd.copy_(q.to(dev))
+    kc, vc = case.pool(dev)
+    out = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    wllm.paged_attention_prefill(out, qd, kc, vc, case.block_tables.to(dev), case.context_lens.to(dev), qsl.to(dev),
+                                 2, case.scale, 16)
+    torch.cuda.synchronize()
+    assert_attention_close(out.cpu(), run_oracle(case, q, qsl), torch.float16, "misaligned q")
+
+
+def test_prefill_long_chunks_sampled(kernel):
     # four sequences, 1024-token chunks after 0..3000 tokens of context: sampled rows
     rng = np.random.default_rng(4)
     prior = rng.integers(0, 3000, size=4)

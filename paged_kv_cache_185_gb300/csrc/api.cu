@@ -1070,7 +1070,7 @@ int prefill_call(const wllm_tensor* out, const wllm_tensor* q, const wllm_tensor
   // WLLM_PREFILL_KERNEL=mma selects the mma.sync kernel
   const bool rows16 = aligned(q->data, 16) && aligned(out->data, 16) && q->stride[0] % 8 == 0 &&
                       q->stride[1] % 8 == 0 && out->stride[0] % 8 == 0 && out->stride[1] % 8 == 0;
-  const bool use_tc = !kv_fp8 && rows16 && !env_is("WLLM_PREFILL_KERNEL", "mma");
+  const bool use_tc = !kv_fp8 && rows16 && scale > 0.f && !env_is("WLLM_PREFILL_KERNEL", "mma");
   cudaError_t e;
   if (use_tc) {
     const int grid_x = prefill_tc_grid_x(T, B, p.group);

@@ -79,6 +79,31 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// try_wait that may suspend the thread (it does not issue meanwhile) until
+// the phase completes or about `hint_ns` have passed.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait whose polls suspend the thread between checks (for waiters
+// that share their SM sub-partition with busy warps).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Wait for phase `parity` of the barrier, giving up after `limit_ns`.
 // Returns false on timeout (the caller records an error and stops).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {

@@ -148,7 +148,7 @@ int launch_prefill(int dtype, int head_dim, bool kv_fp8, const CUtensorMap& kmap
 
 // The same operation on the fifth-generation tensor cores (tcgen05 MMAs with
 // TMEM accumulators): 16-bit caches, head_dim 64 or 128, q/out rows 16-byte
-// aligned (base and strides).  128 query rows per CTA.
+// aligned (base and strides), a positive scale.  256 query rows per CTA.
 int prefill_tc_grid_x(int64_t num_tokens, int64_t num_seqs, int group);
 int launch_prefill_tc(int dtype, int head_dim, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const PrefillParams& p, int grid_x, cudaStream_t stream);

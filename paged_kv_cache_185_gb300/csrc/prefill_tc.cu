@@ -8,37 +8,43 @@
 // token i of sequence b sits at position P = L_b - n_b + i and attends to the
 // cached tokens 0 .. P.  The tiling is this library's design.
 //
-// One CTA owns 128 query rows of one sequence and one kv head -- row r of the
-// sequence's chunk is (token r / G, query head r % G of the kv head's group), so
-// the G heads of a group share every staged K/V byte -- and walks the rows'
-// context in 64-token tiles.  Six warps:
+// One CTA (one per SM) owns 256 query rows of one sequence and one kv head,
+// as two 128-row tiles -- row r of the sequence's chunk is (token r / G, query
+// head r % G of the kv head's group), so the G heads of a group and both tiles
+// share every staged K/V byte -- and walks the rows' context in 128-token kv
+// tiles.  Tensor memory holds, per Q tile, the scores S (128 columns, fp32),
+// over which the softmax writes the weights P (16-bit, two per column), and the
+// output O (head_dim columns).  Ten warps:
 //
-//   warp 0 (producer): reads the block table and stages each tile's K and then
-//     its V (16-row TMA boxes, 128-byte swizzle) into a ring of slots laid out
-//     [head_dim / 64][64 tokens][128 bytes], so that the 8-row groups of a slot
-//     sit 1024 bytes apart, as the MMA descriptors require;
-//   warp 1 (MMA): one thread issues S_j = Q K_j^T (M = 128, N = 64, K = 16 per
-//     instruction; Q and K both K-major) into one of two TMEM buffers, then,
-//     once the softmax has written P_{j-1} to shared memory, O += P_{j-1} V_{j-1}
-//     (M = 128, N = head_dim; V read MN-major straight from its slot); each
-//     group of MMAs completes onto an mbarrier (tcgen05.commit), which also
-//     hands the slot back to the producer.  S_{j+1} is computed while the
-//     softmax works on S_j;
-//   warps 2-5 (softmax): thread r owns row r (TMEM lane r): it loads its row of
-//     Q into shared memory once, then per tile reads its 64 scores from TMEM,
-//     applies the scale and the causal mask, and updates a running maximum that
-//     is only moved when a score exceeds it by more than 8 in the log2 domain
-//     (so weights stay below 2^8; O in TMEM is rescaled only on such a move),
-//     rounds the weights P to the input type, writes them into the
-//     shared-memory A operand of the PV product and adds the ROUNDED weights to
-//     the running sum: numerator and denominator then use the same weights, so
-//     a dominant token whose weight is not exactly 1 (the maximum being stale)
+//   warp 0 (producer): reads the block table and stages each kv tile's K and
+//     then its V (16-row TMA boxes, 128-byte swizzle) into a ring of slots laid
+//     out [head_dim / 64][128 tokens][128 bytes], so that the 8-row groups of a
+//     slot sit 1024 bytes apart, as the MMA descriptors require; rows of the
+//     last kv tile past the context are zeroed once their copy has landed;
+//   warp 1 (MMA): one thread issues, for each Q tile x, S_x = Q_x K^T (M = 128,
+//     N = 128, K = 16 per instruction; Q and K K-major, from shared memory) and
+//     O_x += P_x V (M = 128, N = head_dim; P read from tensor memory, V
+//     MN-major straight from its slot).  S_x of the next kv tile is issued once
+//     O_x += P_x V has completed (it overwrites P_x), so while one Q tile's
+//     softmax runs the tensor core works on the other tile.  It takes the
+//     products of each kind in order but issues whichever is ready first.
+//     Each group of MMAs completes onto an mbarrier (tcgen05.commit), which
+//     also hands a slot back to the producer once both tiles are done with it;
+//   warps 2-5 and 6-9 (softmax of Q tile 0 and 1): thread r owns row r of its
+//     tile (TMEM lane r): it loads its row of Q into shared memory once, then
+//     per kv tile reads its 128 scores from TMEM, applies the causal mask and
+//     updates a running maximum that is only moved when a scaled score exceeds
+//     it by more than 8 in the log2 domain (so weights stay below 2^8; O is
+//     rescaled in TMEM only on such a move -- O is at rest then, its last
+//     product having completed before these scores were computed), rounds the
+//     weights exp2(scale * s - m) (one FFMA and one exp2 each) to the input
+//     type, stores them over the scores, and adds the ROUNDED weights to the
+//     running sum: numerator and denominator then use the same weights, so a
+//     dominant token whose weight is not exactly 1 (the maximum being stale)
 //     adds no rounding error of its own.  At the end it divides O by the
 //     running sum and stores the row.
 //
-// Two CTAs fit on an SM (shared memory ~99 KB each, 256 TMEM columns each: S0,
-// S1 and O), so one CTA's softmax overlaps the other's tensor-core work.  Every
-// mbarrier wait is bounded; on a timeout the CTA records the error, waits
+// Every wait is bounded; on a timeout the CTA records the error, waits
 // (bounded) for its copies and MMAs in flight, frees its TMEM and returns.
 #include <type_traits>
 
@@ -50,28 +56,34 @@ namespace wllm {
 
 namespace {
 
-constexpr int kTcRows = 128;        // query rows per CTA (one M = 128 tile)
-constexpr int kTcKv = 64;           // kv tokens per tile
-constexpr int kTcThreads = 6 * 32;  // producer, MMA, four softmax warps
-constexpr float kTcRescale = 8.f;   // the running maximum moves by more than 2^8 only
+constexpr int kTcTileRows = 128;                      // rows of one Q tile (M = 128)
+constexpr int kTcTiles = 2;                           // Q tiles per CTA
+constexpr int kTcRows = kTcTileRows * kTcTiles;       // query rows per CTA
+constexpr int kTcKv = 128;                            // kv tokens per kv tile
+constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;   // producer, MMA, four softmax warps per Q tile
+constexpr float kTcRescale = 8.f;                     // the running maximum moves by more than 8 (log2) only
 
 template <int D>
 struct TcShape {
-  static constexpr int kChunks = D / 64;               // 128-byte chunks of a 16-bit row
-  static constexpr int kQBytes = kTcRows * D * 2;      // [chunk][128 rows][128 B]
-  static constexpr int kPBytes = kTcRows * kTcKv * 2;  // [128 rows][128 B]
-  static constexpr int kSlotBytes = kTcKv * D * 2;     // [chunk][64 tokens][128 B]
-  static constexpr int kSlots = D == 64 ? 8 : 3;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kQBytes + kPBytes + kSlots * kSlotBytes + kBarBytes;
-  static constexpr uint32_t kTmemCols = 256;
-  static constexpr int kS0 = 0, kS1 = 64, kO = 128;  // TMEM columns: scores (two buffers), output
+  static constexpr int kChunks = D / 64;                     // 128-byte chunks of a 16-bit row
+  static constexpr int kQTileBytes = kTcTileRows * D * 2;    // [chunk][128 rows][128 B]
+  static constexpr int kSlotBytes = kTcKv * D * 2;           // [chunk][128 tokens][128 B]
+  static constexpr int kChunkStride = kTcKv * 128;           // bytes between the chunks of a slot
+  static constexpr int kBarBytes = 512;
+  static constexpr int kFixed = 1024 + kTcTiles * kQTileBytes + kBarBytes;
+  static constexpr int kSlotsRaw = (232448 - kFixed) / kSlotBytes;  // 227 KB of dynamic shared memory
+  static constexpr int kSlots = kSlotsRaw > 16 ? 16 : kSlotsRaw;
+  static constexpr int kSmem = kFixed + kSlots * kSlotBytes;
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns of Q tile x start at x * kTileCols: scores S (P over its
+  // first 64 columns), output O
+  static constexpr int kTileCols = 256;
+  static constexpr int kS = 0, kO = 128;
 };
-// At most two CTAs fit on an SM, so their 2 x 256 TMEM columns always fit and
-// an allocation never waits.
-static_assert(3 * (TcShape<64>::kSmem + 1024) > 233472 && 3 * (TcShape<128>::kSmem + 1024) > 233472,
-              "a third resident CTA would contend for TMEM");
-static_assert(2 * (TcShape<128>::kSmem + 1024) <= 233472, "two CTAs per SM");
+// One CTA per SM, so the 512 TMEM columns are always free to allocate.
+static_assert(2 * (TcShape<64>::kSmem + 1024) > 233472 && 2 * (TcShape<128>::kSmem + 1024) > 233472,
+              "a second resident CTA would contend for TMEM");
+static_assert(TcShape<128>::kSlots >= 5 && TcShape<64>::kSlots >= 5, "at least two kv tiles in flight");
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -100,7 +112,7 @@ __device__ __forceinline__ float pair_sum<__half>(uint32_t w) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                             const PrefillParams p) {
   using TS = TcShape<D>;
@@ -108,26 +120,25 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;
-  uint8_t* p_s = q_s + TS::kQBytes;
-  uint8_t* ring = p_s + TS::kPBytes;
+  uint8_t* q_s = smem;                              // [2][Q tile]
+  uint8_t* ring = q_s + kTcTiles * TS::kQTileBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + R * TS::kSlotBytes);
   uint64_t* empty = full + R;
-  uint64_t* sfull = empty + R;   // [2] S buffer written (MMA -> softmax)
-  uint64_t* sfree = sfull + 2;   // [2] S buffer read (softmax -> MMA)
-  uint64_t* pfull = sfree + 2;   // P written, O rescaled (softmax -> MMA)
-  uint64_t* odone = pfull + 1;   // a PV product done (MMA -> softmax)
-  uint64_t* qfull = odone + 1;   // Q written (softmax -> MMA)
-  uint64_t* fin = qfull + 1;     // every MMA of the CTA done
+  uint64_t* sfull = empty + R;     // [tile] S written (MMA -> softmax)
+  uint64_t* pfull = sfull + 2;     // [tile] P written, O rescaled (softmax -> MMA)
+  uint64_t* pvdone = pfull + 2;    // [tile] the PV product done (MMA -> MMA, softmax)
+  uint64_t* vzero = pvdone + 2;    // the last kv tile's V rows past the context zeroed (producer -> MMA)
+  uint64_t* qfull = vzero + 1;     // Q written (softmax -> MMA)
+  uint64_t* fin = qfull + 1;       // every MMA of the CTA done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
-  int* info = reinterpret_cast<int*>(tslot + 1);  // [0] sequence (-1: none), [1] its row tile
+  int* info = reinterpret_cast<int*>(tslot + 1);  // [0] sequence (-1: none), [1] its row block
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int kvh = blockIdx.y;
 
-  // ---- which (sequence, row tile) this CTA owns: sequence b owns
-  // ceil(n_b * G / 128) consecutive slots of blockIdx.x
+  // ---- which (sequence, row block) this CTA owns: sequence b owns
+  // ceil(n_b * G / 256) consecutive slots of blockIdx.x
   if (warp == 0) {
     int seq = -1, tile = 0, base = 0;
     for (int b0 = 0; b0 < p.num_seqs && seq < 0; b0 += 32) {
@@ -161,13 +172,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         mbar_init(smem_u32(full + s), 1);
         mbar_init(smem_u32(empty + s), 1);
       }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(smem_u32(sfull + i), 1);
-        mbar_init(smem_u32(sfree + i), 4);
+      for (int x = 0; x < kTcTiles; ++x) {
+        mbar_init(smem_u32(sfull + x), 1);
+        mbar_init(smem_u32(pfull + x), 4);
+        mbar_init(smem_u32(pvdone + x), 1);
       }
-      mbar_init(smem_u32(pfull), 4);
-      mbar_init(smem_u32(odone), 1);
-      mbar_init(smem_u32(qfull), 4);
+      mbar_init(smem_u32(vzero), 1);
+      mbar_init(smem_u32(qfull), 4 * kTcTiles);
       mbar_init(smem_u32(fin), 1);
       fence_mbar_init();
     }
@@ -179,9 +190,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
 
-  // ---- the tile's rows and the context they see (uniform over the CTA)
+  // ---- the block's rows and the context they see (uniform over the CTA)
   const int b = info[0];
-  int n_tiles = 0, row0 = 0, n_rows = 0, pos0 = 0, kv_end = 0, s0 = 0;
+  int n_rows = 0, row0 = 0, pos0 = 0, s0 = 0;
+  int nt[kTcTiles] = {0, 0};  // kv tiles each Q tile needs
+  int kv_end = 0;             // tokens any row of the block sees
   if (b >= 0) {
     const int l_max = p.max_blocks * p.block_size;
     s0 = p.query_start_loc[b];
@@ -197,14 +210,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       n_rows = n * G;
       row0 = info[1] * kTcRows;
-      if (row0 < n_rows) {  // (not so only when n was clamped, error already flagged)
-        const int row_last = min(n_rows, row0 + kTcRows) - 1;
-        pos0 = L - n;
-        kv_end = pos0 + row_last / G + 1;
-        n_tiles = (kv_end + kTcKv - 1) / kTcKv;
+      pos0 = L - n;
+#pragma unroll
+      for (int x = 0; x < kTcTiles; ++x) {  // (no rows only when n was clamped, error already flagged)
+        const int rx = row0 + x * kTcTileRows;
+        if (rx < n_rows) {
+          const int end_x = pos0 + (min(n_rows, rx + kTcTileRows) - 1) / G + 1;
+          nt[x] = (end_x + kTcKv - 1) / kTcKv;
+          kv_end = max(kv_end, end_x);
+        }
       }
     }
   }
+  const int n_tiles = max(nt[0], nt[1]);
+  const bool v_tail = n_tiles * kTcKv > kv_end;  // the last kv tile reaches past the context
 
   // one lane waits, the warp learns the outcome
   auto wait_warp = [&](uint64_t* bar, int parity) -> bool {
@@ -220,14 +239,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
     }
+    constexpr int kSub = kTcKv / 16;  // 16-token sub-tiles of a kv tile
     const int32_t* bt_row = p.block_tables + static_cast<int64_t>(b) * p.bt_stride;
     const bool two = p.log2_bs < 4;  // 8-token blocks: two 8-row boxes per 16 tokens
     int issued = 0;                  // slot uses whose copies were issued
     for (int j = 0; ok && j < n_tiles; ++j) {
-      // lanes 0..3: the table entries of the tile's four 16-token sub-tiles
+      // lanes 0..7: the table entries of the tile's 16-token sub-tiles
       int e0 = 0, e1 = 0;
       const int tj = j * kTcKv + 16 * lane;
-      if (lane < 4 && tj < kv_end) {
+      if (lane < kSub && tj < kv_end) {
         e0 = bt_row[tj >> p.log2_bs];
         if (two && tj + 8 < kv_end) e1 = bt_row[(tj >> p.log2_bs) + 1];
         if (e0 < 0 || e0 >= p.num_blocks || e1 < 0 || e1 >= p.num_blocks) {
@@ -236,12 +256,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           e1 = (e1 < 0 || e1 >= p.num_blocks) ? 0 : e1;
         }
       }
-      int ent0[4], ent1[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        ent0[jj] = __shfl_sync(kFullMask, e0, jj);
-        ent1[jj] = __shfl_sync(kFullMask, e1, jj);
-      }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {  // K, then V
         const int c = 2 * j + half, s = c % R;
@@ -249,34 +263,51 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           ok = false;
           break;
         }
-        if (lane == 0) {
-          const CUtensorMap* map = half ? &vmap : &kmap;
-          const uint32_t slot = smem_u32(ring + s * TS::kSlotBytes);
-          const uint32_t bar = smem_u32(full + s);
-          uint32_t bytes = 0;
+        const CUtensorMap* map = half ? &vmap : &kmap;
+        const uint32_t slot = smem_u32(ring + s * TS::kSlotBytes);
+        const uint32_t bar = smem_u32(full + s);
+        // lane jj < kSub issues sub-tile jj's boxes after lane 0 set the byte count
+        const int t = j * kTcKv + 16 * lane;
+        const bool live = lane < kSub && t < kv_end;
+        const uint32_t my_bytes = live ? ((two && !(t + 8 < kv_end)) ? 8u : 16u) * 128u * TS::kChunks : 0u;
+        uint32_t bytes = my_bytes;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int t = j * kTcKv + 16 * jj;
-            if (t < kv_end) bytes += ((two && !(t + 8 < kv_end)) ? 8u : 16u) * 128u * TS::kChunks;
-          }
-          mbar_arrive_expect_tx(bar, bytes);
+        for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(kFullMask, bytes, off);
+        if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+        __syncwarp();
+        if (live) {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int t = j * kTcKv + 16 * jj;
-            if (t >= kv_end) continue;
-#pragma unroll
-            for (int cb = 0; cb < TS::kChunks; ++cb) {
-              const uint32_t dst = slot + cb * (kTcKv * 128) + jj * 2048;
-              if (!two) {
-                tma_load_3d(dst, map, bar, cb * 64, kvh * p.block_size + (t & (p.block_size - 1)), ent0[jj]);
-              } else {
-                tma_load_3d(dst, map, bar, cb * 64, kvh * p.block_size, ent0[jj]);
-                if (t + 8 < kv_end) tma_load_3d(dst + 1024, map, bar, cb * 64, kvh * p.block_size, ent1[jj]);
-              }
+          for (int cb = 0; cb < TS::kChunks; ++cb) {
+            const uint32_t dst = slot + cb * TS::kChunkStride + lane * 2048;
+            if (!two) {
+              tma_load_3d(dst, map, bar, cb * 64, kvh * p.block_size + (t & (p.block_size - 1)), e0);
+            } else {
+              tma_load_3d(dst, map, bar, cb * 64, kvh * p.block_size, e0);
+              if (t + 8 < kv_end) tma_load_3d(dst + 1024, map, bar, cb * 64, kvh * p.block_size, e1);
             }
           }
         }
         ++issued;
+        if (half == 1 && j == n_tiles - 1 && v_tail) {
+          // V rows at or past kv_end were never staged (or hold slots past the
+          // sequence's end): once the copy has landed, zero them, since a zero
+          // weight does not cancel a NaN
+          if (!wait_warp(full + s, (c / R) & 1)) {
+            ok = false;
+            break;
+          }
+          const int r0 = kv_end - j * kTcKv;
+          uint8_t* vs = ring + s * TS::kSlotBytes;
+          for (int idx = lane; idx < (kTcKv - r0) * TS::kChunks * 8; idx += 32) {
+            const int row = r0 + idx / (TS::kChunks * 8);
+            const int rem = idx - (idx / (TS::kChunks * 8)) * (TS::kChunks * 8);
+            *reinterpret_cast<uint4*>(vs + (rem >> 3) * TS::kChunkStride + row * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(vzero));
+        }
       }
     }
     // every copy still in flight lands before the CTA may leave
@@ -284,167 +315,178 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       if (!wait_warp(full + c % R, (c / R) & 1)) ok = false;
   } else if (warp == 1 && n_tiles > 0) {
     // --------------------------------- MMA ----------------------------------
-    constexpr uint32_t kIdS = tc::f16_idesc(kBf16, false, false, kTcRows, kTcKv);
-    constexpr uint32_t kIdO = tc::f16_idesc(kBf16, false, true, kTcRows, D);
-    const uint32_t q_a = smem_u32(q_s), p_a = smem_u32(p_s), ring_a = smem_u32(ring);
-    auto issue_pv = [&](int i) -> bool {
-      if (!wait_warp(pfull, i & 1)) return false;
-      const int c = 2 * i + 1, s = c % R;
-      if (!wait_warp(full + s, (c / R) & 1)) return false;
-      const int t0 = i * kTcKv;
-      if (t0 + kTcKv > kv_end) {
-        // V rows at or past kv_end were never staged (or hold slots past the
-        // sequence's end): zero them, since P = 0 there does not cancel NaN
-        const int r0 = kv_end - t0;
-        uint8_t* slot = ring + s * TS::kSlotBytes;
-        for (int idx = lane; idx < (kTcKv - r0) * TS::kChunks * 8; idx += 32) {
-          const int row = r0 + idx / (TS::kChunks * 8);
-          const int rem = idx - (idx / (TS::kChunks * 8)) * (TS::kChunks * 8);
-          *reinterpret_cast<uint4*>(slot + (rem >> 3) * (kTcKv * 128) + row * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc::f16_idesc(kBf16, false, false, kTcTileRows, kTcKv);
+      constexpr uint32_t kIdO = tc::f16_idesc(kBf16, false, true, kTcTileRows, D);
+      const uint32_t q_a = smem_u32(q_s), ring_a = smem_u32(ring);
+      // the operations of one kind in order: kv tile by kv tile, Q tile 0 then
+      // 1, skipping Q tiles that need fewer kv tiles
+      const int m2 = min(nt[0], nt[1]);
+      const int total = nt[0] + nt[1];
+      auto op_at = [&](int k, int& j, int& x) {
+        if (k < 2 * m2) {
+          j = k >> 1;
+          x = k & 1;
+        } else {
+          j = m2 + (k - 2 * m2);
+          x = nt[0] > nt[1] ? 0 : 1;
         }
-        tc::fence_async_smem();
-        __syncwarp();
-      }
-      if (lane == 0) {
-        tc::fence_after_sync();
-        const uint32_t v0 = ring_a + s * TS::kSlotBytes;
+      };
+      // the last operation of its kind on kv tile j (then the slot can go back)
+      auto last_on_tile = [&](int j, int x) { return x == 1 || j >= nt[1]; };
+      ok = mbar_wait_bounded(smem_u32(qfull), 0, p.wait_limit_ns);
+      int ks = 0, kp = 0;  // next S product, next PV product
+      uint64_t t_idle = 0;
+      int idle = 0;        // polls since the last issue (the timer is read every 64)
+      while (ok && kp < total) {
+        bool did = false;
+        if (ks < total) {
+          int j, x;
+          op_at(ks, j, x);
+          const int c = 2 * j, s = c % R;
+          // S_x(j) overwrites P_x(j-1): O_x += P_x(j-1) V must be done
+          if (mbar_test_wait(smem_u32(full + s), (c / R) & 1) &&
+              (j == 0 || mbar_test_wait(smem_u32(pvdone + x), (j - 1) & 1))) {
+            tc::fence_after_sync();
+            const uint64_t qd = tc::sw128_desc(q_a + x * TS::kQTileBytes, 16, 1024);
+            const uint64_t kd = tc::sw128_desc(ring_a + s * TS::kSlotBytes, 16, 1024);
+            const uint32_t d = tmem + x * TS::kTileCols + TS::kS;
 #pragma unroll
-        for (int kk = 0; kk < kTcKv / 16; ++kk)
-          tc::mma_f16(tmem + TS::kO, tc::sw128_desc(p_a + kk * 32, 16, 1024),
-                      tc::sw128_desc(v0 + kk * 2048, kTcKv * 128, 1024), kIdO, (i > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(smem_u32(odone));
-        tc::commit(smem_u32(empty + s));
-      }
-      __syncwarp();
-      return true;
-    };
-    ok = wait_warp(qfull, 0);
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int c = 2 * j, s = c % R;
-      ok = wait_warp(full + s, (c / R) & 1) && wait_warp(sfree + (j & 1), ((j >> 1) & 1) ^ 1);
-      if (!ok) break;
-      if (lane == 0) {
-        tc::fence_after_sync();
-        const uint32_t k0 = ring_a + s * TS::kSlotBytes;
-        const uint32_t d = tmem + ((j & 1) ? TS::kS1 : TS::kS0);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int kc = ks >> 2, kin = ks & 3;
-          tc::mma_f16(d, tc::sw128_desc(q_a + kc * (kTcRows * 128) + kin * 32, 16, 1024),
-                      tc::sw128_desc(k0 + kc * (kTcKv * 128) + kin * 32, 16, 1024), kIdS, ks > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // descriptor start addresses advance in 16-byte units
+              const uint32_t qo = ((kk >> 2) * kTcTileRows * 128 + (kk & 3) * 32) >> 4;
+              const uint32_t ko = ((kk >> 2) * TS::kChunkStride + (kk & 3) * 32) >> 4;
+              tc::mma_f16(d, qd + qo, kd + ko, kIdS, kk > 0 ? 1u : 0u);
+            }
+            tc::commit(smem_u32(sfull + x));
+            if (last_on_tile(j, x)) tc::commit(smem_u32(empty + s));
+            ++ks;
+            did = true;
+          }
         }
-        tc::commit(smem_u32(sfull + (j & 1)));
-        tc::commit(smem_u32(empty + s));
+        if (kp < ks) {
+          int j, x;
+          op_at(kp, j, x);
+          const int c = 2 * j + 1, s = c % R;
+          if (mbar_test_wait(smem_u32(pfull + x), j & 1) && mbar_test_wait(smem_u32(full + s), (c / R) & 1) &&
+              (!(v_tail && j == n_tiles - 1) || mbar_test_wait(smem_u32(vzero), 0))) {
+            tc::fence_after_sync();
+            const uint64_t vd = tc::sw128_desc(ring_a + s * TS::kSlotBytes, TS::kChunkStride, 1024);
+            const uint32_t d = tmem + x * TS::kTileCols + TS::kO;
+            const uint32_t pa = tmem + x * TS::kTileCols + TS::kS;  // P: 8 columns per 16 tokens
+#pragma unroll
+            for (int kk = 0; kk < kTcKv / 16; ++kk)
+              tc::mma_f16_ts(d, pa + kk * 8, vd + ((kk * 2048) >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+            tc::commit(smem_u32(pvdone + x));
+            if (last_on_tile(j, x)) tc::commit(smem_u32(empty + s));
+            ++kp;
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if ((++idle & 63) == 0) {  // a bounded wait: no issue for wait_limit_ns gives up
+          const uint64_t now = global_timer_ns();
+          if (idle == 64) t_idle = now;
+          else if (now - t_idle > p.wait_limit_ns) ok = false;
+        }
       }
-      __syncwarp();
-      if (j > 0) ok = issue_pv(j - 1);
+      tc::commit(smem_u32(fin));  // every MMA issued above, on every path
     }
-    if (ok) ok = issue_pv(n_tiles - 1);
-    if (lane == 0) tc::commit(smem_u32(fin));  // every MMA issued above, on every path
     __syncwarp();
+    ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
   } else if (warp >= 2 && n_tiles > 0) {
     // ------------------------------- softmax --------------------------------
-    const int quarter = warp & 3;           // the TMEM lanes this warp reaches
-    const int r = quarter * 32 + lane;      // this thread's row of the tile
-    const int rowg = row0 + r;
+    const int x = (warp - 2) >> 2;           // this warp's Q tile
+    const int quarter = warp & 3;            // the TMEM lanes this warp reaches
+    const int r = quarter * 32 + lane;       // this thread's row of the tile
+    const int rowg = row0 + x * kTcTileRows + r;
     const bool valid = rowg < n_rows;
     const int tok = valid ? rowg / G : 0;
     const int gh = valid ? rowg - tok * G : 0;
     const int pos = valid ? pos0 + tok : 0;  // padding rows see token 0 only (output dropped)
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t trow = tmem + x * TS::kTileCols + (static_cast<uint32_t>(quarter * 32) << 16);
     {
+      uint8_t* qx = q_s + x * TS::kQTileBytes;
       const T* qrow = reinterpret_cast<const T*>(p.q) + static_cast<int64_t>(s0 + tok) * p.q_st +
                       static_cast<int64_t>(kvh * G + gh) * p.q_sh;
 #pragma unroll
       for (int c16 = 0; c16 < D / 8; ++c16) {
         const uint4 v = valid ? *reinterpret_cast<const uint4*>(qrow + c16 * 8) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(q_s + (c16 >> 3) * (kTcRows * 128) + r * 128 + (((c16 & 7) ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(qx + (c16 >> 3) * (kTcTileRows * 128) + r * 128 + (((c16 & 7) ^ (r & 7)) << 4)) = v;
       }
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(qfull));
     }
+    const float sl2 = p.scale_log2;  // positive (host-checked): the largest score scales to the largest
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!wait_warp(sfull + (j & 1), (j >> 1) & 1)) {
+    const int ntx = x ? nt[1] : nt[0];
+    for (int j = 0; j < ntx; ++j) {
+      if (!wait_warp(sfull + x, j & 1)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      float x[2][32];
-      const uint32_t sc = trow + ((j & 1) ? TS::kS1 : TS::kS0);
-      tc::ld32(sc, x[0]);
-      tc::ld32(sc + 32, x[1]);
+      float v[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc::ld32(trow + TS::kS + 32 * q, v[q]);
       tc::wait_ld();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(sfree + (j & 1)));
       const int t0 = j * kTcKv;
-      float mx = -INFINITY;
-      if (t0 + kTcKv - 1 <= pos) {
+      if (t0 + kTcKv - 1 > pos) {  // the causal edge (and tokens past kv_end, whose K was never staged)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[h][i] *= p.scale_log2;
-            mx = fmaxf(mx, x[h][i]);
-          }
-      } else {  // the causal edge (and tokens past kv_end, whose K was never staged)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[h][i] = t0 + 32 * h + i <= pos ? x[h][i] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, x[h][i]);
-          }
+          for (int i = 0; i < 32; ++i) v[q][i] = t0 + 32 * q + i <= pos ? v[q][i] : -INFINITY;
       }
+      float mxs[8];  // eight independent maxima of the raw scores: a short dependency chain
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mxs[k] = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mxs[i & 7] = fmaxf(mxs[i & 7], v[q][i]);
+      const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
       float alpha = 1.f;
-      if (mx > m + kTcRescale) {  // also the first tile (m = -inf): token 0 is always seen
+      if (mx > m + kTcRescale) {  // also the first kv tile (m = -inf): token 0 is always seen
         alpha = exp2f(m - mx);
         m = mx;
       }
-      float sum = 0.f;
-      uint32_t pk[32];
+      const float nm = -m;
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int hq = 0; hq < 2; ++hq) {  // 64 scores -> 32 packed weights -> one TMEM store
+        float w[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t w = pack2<T>(exp2f(x[h][2 * i] - m), exp2f(x[h][2 * i + 1] - m));
-          sum += pair_sum<T>(w);  // the rounded weights the PV product uses
-          pk[16 * h + i] = w;
+        for (int i = 0; i < 32; ++i) {
+          const int q = 2 * hq + (i >> 4), e = 2 * (i & 15);
+          const uint32_t pw = pack2<T>(exp2f(fmaf(v[q][e], sl2, nm)), exp2f(fmaf(v[q][e + 1], sl2, nm)));
+          sums[i & 3] += pair_sum<T>(pw);  // the rounded weights the PV product uses
+          w[i] = __uint_as_float(pw);
         }
-      l = l * alpha + sum;
-      if (j > 0) {  // PV_{j-1} has read P and written O
-        if (!wait_warp(odone, (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        if (__any_sync(kFullMask, alpha != 1.f)) {
+        tc::st32(trow + TS::kS + 32 * hq, w);
+      }
+      l = l * alpha + ((sums[0] + sums[1]) + (sums[2] + sums[3]));
+      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+        // O is at rest: its last product completed before S_j was issued
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tc::ld32(trow + TS::kO + 32 * c, o);
-            tc::wait_ld();
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tc::ld32(trow + TS::kO + 32 * c, o);
+          tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc::st32(trow + TS::kO + 32 * c, o);
-          }
-          tc::wait_st();
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tc::st32(trow + TS::kO + 32 * c, o);
         }
       }
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(p_s + r * 128 + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      tc::fence_async_smem();
+      tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(pfull));
+      if (lane == 0) mbar_arrive(smem_u32(pfull + x));
     }
-    if (ok) ok = wait_warp(fin, 0);
-    if (ok) {
+    if (ok && ntx > 0) ok = wait_warp(pvdone + x, (ntx - 1) & 1);  // this tile's last PV product
+    if (ok && ntx > 0) {
       tc::fence_after_sync();
       const float inv = 1.f / l;
       T* orow = reinterpret_cast<T*>(p.out) + static_cast<int64_t>(s0 + tok) * p.o_st +
@@ -496,7 +538,7 @@ int launch_tc_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const Prefi
 }  // namespace
 
 int prefill_tc_grid_x(int64_t num_tokens, int64_t num_seqs, int group) {
-  // an upper bound on the row tiles: sum_b ceil(n_b G / 128) <= ceil(T G / 128) + B
+  // an upper bound on the row blocks: sum_b ceil(n_b G / 256) <= ceil(T G / 256) + B
   return static_cast<int>((num_tokens * group + kTcRows - 1) / kTcRows + num_seqs);
 }
 

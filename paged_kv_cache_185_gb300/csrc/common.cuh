@@ -238,6 +238,15 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float hi, float lo) {
   return y;
 }
 
+// 2^x by the SFU's approximate exponential (ex2.approx.ftz: one SFU
+// operation, subnormal results flushed to zero); for softmax weights that are
+// rounded to 16 bits afterwards.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

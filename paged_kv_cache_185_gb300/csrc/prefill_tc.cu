@@ -37,7 +37,7 @@
 //     it by more than 8 in the log2 domain (so weights stay below 2^8; O is
 //     rescaled in TMEM only on such a move -- O is at rest then, its last
 //     product having completed before these scores were computed), rounds the
-//     weights exp2(scale * s - m) (one FFMA and one exp2 each) to the input
+//     weights exp2(scale * s - m) (one FFMA and one SFU exp2 each) to the input
 //     type, stores them over the scores, and adds the ROUNDED weights to the
 //     running sum: numerator and denominator then use the same weights, so a
 //     dominant token whose weight is not exactly 1 (the maximum being stale)
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                    fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
       float alpha = 1.f;
       if (mx > m + kTcRescale) {  // also the first kv tile (m = -inf): token 0 is always seen
-        alpha = exp2f(m - mx);
+        alpha = ex2_approx(m - mx);
         m = mx;
       }
       const float nm = -m;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int q = 2 * hq + (i >> 4), e = 2 * (i & 15);
-          const uint32_t pw = pack2<T>(exp2f(fmaf(v[q][e], sl2, nm)), exp2f(fmaf(v[q][e + 1], sl2, nm)));
+          const uint32_t pw = pack2<T>(ex2_approx(fmaf(v[q][e], sl2, nm)), ex2_approx(fmaf(v[q][e + 1], sl2, nm)));
           sums[i & 3] += pair_sum<T>(pw);  // the rounded weights the PV product uses
           w[i] = __uint_as_float(pw);
         }

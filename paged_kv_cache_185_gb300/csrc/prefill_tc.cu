@@ -98,17 +98,32 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Sum of the two 16-bit values of a pair (exact in fp32).
+// acc + lo + hi for the two 16-bit values of a pair, each added by one
+// mixed-precision add (the 16-bit operand widened exactly, fp32 result).
 template <typename T>
-__device__ __forceinline__ float pair_sum(uint32_t w);
+__device__ __forceinline__ float add_pair(float acc, uint32_t w);
 template <>
-__device__ __forceinline__ float pair_sum<__nv_bfloat16>(uint32_t w) {
-  return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+__device__ __forceinline__ float add_pair<__nv_bfloat16>(float acc, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w));
+  return acc;
 }
 template <>
-__device__ __forceinline__ float pair_sum<__half>(uint32_t w) {
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
-  return f.x + f.y;
+__device__ __forceinline__ float add_pair<__half>(float acc, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w));
+  return acc;
+}
+
+// max(a, b, c) in one three-input max.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 template <typename T, int D>
@@ -445,7 +460,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mxs[i & 7] = fmaxf(mxs[i & 7], v[q][i]);
+        for (int i = 0; i < 32; i += 2) mxs[(i >> 1) & 7] = max3f(mxs[(i >> 1) & 7], v[q][i], v[q][i + 1]);
       const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
                                    fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
       float alpha = 1.f;
@@ -462,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < 32; ++i) {
           const int q = 2 * hq + (i >> 4), e = 2 * (i & 15);
           const uint32_t pw = pack2<T>(ex2_approx(fmaf(v[q][e], sl2, nm)), ex2_approx(fmaf(v[q][e + 1], sl2, nm)));
-          sums[i & 3] += pair_sum<T>(pw);  // the rounded weights the PV product uses
+          sums[i & 3] = add_pair<T>(sums[i & 3], pw);  // the rounded weights the PV product uses
           w[i] = __uint_as_float(pw);
         }
         tc::st32(trow + TS::kS + 32 * hq, w);

@@ -138,8 +138,10 @@ int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value,
  * the device (split-KV); this uses the device workspace (see below).  With
  * F16/BF16 the partitions of a sequence are merged inside the same
  * (cooperative) launch as soon as all of them are done -- per-sequence
- * counters in the workspace, waits bounded in time -- or by a second kernel
- * when the environment variable WLLM_SEPARATE_COMBINE=1 is set.  With a
+ * counters in the workspace, waits bounded in time -- for batches of up to
+ * 4096 query rows (B * Hq), and by a second kernel for larger batches; the
+ * environment variable WLLM_SEPARATE_COMBINE=1 (or 0) forces the second
+ * kernel (or the merge inside the launch).  With a
  * caller workspace set (wllm_set_workspace) the call allocates nothing and can
  * be captured in a CUDA graph.
  * A block-table entry outside [0, N_b) or a length above M_b*bs is clamped on

@@ -328,19 +328,19 @@ int choose_partition_grid(int64_t num_seqs, int64_t units_per_part, int64_t toke
 // Persistent kernel: units are taken dynamically, so what matters is that a
 // unit is small against one CTA's share of the work, and that a sequence is
 // not cut into so many partitions that merging them costs more than the
-// balance gains.  The largest power of two in [256, 4096] that gives >= 8
+// balance gains.  The largest power of two in [512, 4096] that gives >= 8
 // units per CTA when sequences are half as long as the table allows (lengths
 // are on the device; the table width is all the host knows), but at most 128
 // partitions per sequence.  Measured on GB300 over P = 128..4096 on the
-// TinyLlama / Llama-2-7B / Qwen2.5-7B / long-context workloads: 8 units per
-// CTA picks 256 / 4096 / 1024 / 1024 tokens, within 2% of the best partition
-// size of each.
+// TinyLlama / Llama-2-7B / Qwen2.5-7B / long-context workloads: this picks
+// 512 / 4096 / 1024 / 1024 tokens; on the small TinyLlama-shaped batch 512
+// beats 256 by ~8% (fewer partials to merge at the end of the launch).
 int choose_partition_persistent(int64_t num_seqs, int64_t units_per_part, int64_t tokens_max, int64_t n_ctas) {
   long long forced = env_int("WLLM_PARTITION_TOKENS", 0);
   if (forced > 0) return static_cast<int>((forced + 15) / 16 * 16);
   const int64_t est = tokens_max / 2 > 0 ? tokens_max / 2 : 1;
-  int64_t P = 256;
-  for (int64_t cand = 4096; cand >= 256; cand >>= 1)
+  int64_t P = 512;
+  for (int64_t cand = 4096; cand >= 512; cand >>= 1)
     if (num_seqs * units_per_part * ((est + cand - 1) / cand) >= 8 * n_ctas) {
       P = cand;
       break;
@@ -812,9 +812,15 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
     if (e != cudaSuccess) return cuda_fail(e, "check_decode launch");
     if ((rc = collect_device_errors(s, st, "paged_attention_decode"))) return rc;
   }
-  // split partitions are merged inside the (cooperative) launch, overlapped
-  // with the decode, unless asked otherwise
-  const bool separate_kernel = env_flag("WLLM_SEPARATE_COMBINE");
+  // Split partitions are merged inside the (cooperative) launch, overlapped
+  // with the decode, for batches of up to 4096 query rows, and by a second
+  // kernel for larger ones: measured on GB300, merging in the launch is ahead
+  // for few rows with many partitions (long contexts: 256 rows, up to 105
+  // partitions each) and behind for many rows (a 7168-row shared-prefix batch,
+  // where the launch's bookkeeping of finished units costs more than a second
+  // kernel).  WLLM_SEPARATE_COMBINE=1 / 0 forces one or the other.
+  const char* sc = std::getenv("WLLM_SEPARATE_COMBINE");
+  const bool separate_kernel = (sc != nullptr && sc[0] != '\0') ? std::strcmp(sc, "0") != 0 : a.B * a.hq > 4096;
   const DecodePlan first = make_plan(a.dt, std::min<int64_t>(a.B, kPersistentMaxSeqs), a.hq, a.hkv, a.d, a.mb,
                                      a.bs, a.q_bulk_ok, s->num_sms, a.kv_fp8);
   const int64_t slice = first.persistent ? kPersistentMaxSeqs : a.B;

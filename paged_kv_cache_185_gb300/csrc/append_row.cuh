@@ -16,6 +16,27 @@ __device__ __forceinline__ void append_row(const AppendParams& p, int64_t row, i
   const int h = static_cast<int>(row - static_cast<int64_t>(t) * p.num_kv_heads);
   const int64_t slot = p.slots_are_i64 ? static_cast<const int64_t*>(p.slots)[t]
                                        : static_cast<int64_t>(static_cast<const int32_t*>(p.slots)[t]);
+  // 16-bit rows of up to 256 bytes (the common case): this lane's unit of the
+  // K or V row is loaded together with the slot, one memory round trip
+  if (p.vec16 && !p.kv_fp8 && (p.row_bytes >> 4) <= 16) {  // one 16-byte unit of K or V per lane
+    const int n = p.row_bytes >> 4;
+    const bool mine = lane < 2 * n;
+    const int u = lane < n ? lane : lane - n;
+    const uint8_t* src = (lane < n ? p.key + t * p.key_st : p.value + t * p.val_st) +
+                         static_cast<int64_t>(h) * (lane < n ? p.key_sh : p.val_sh);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (mine) v = reinterpret_cast<const uint4*>(src)[u];
+    if (slot < 0) return;  // padding token
+    if (slot >= p.num_slots) {
+      if (lane == 0) atomicOr(p.err, kErrSlot);
+      return;
+    }
+    const int64_t blk = slot >> p.log2_bs;
+    const int64_t off = slot & ((int64_t(1) << p.log2_bs) - 1);
+    const int64_t dst = (((blk * p.num_kv_heads + h) << p.log2_bs) + off) * p.row_bytes;
+    if (mine) reinterpret_cast<uint4*>((lane < n ? p.k_cache : p.v_cache) + dst)[u] = v;
+    return;
+  }
   if (slot < 0) return;  // padding token
   if (slot >= p.num_slots) {
     if (lane == 0) atomicOr(p.err, kErrSlot);

@@ -49,31 +49,35 @@ namespace wllm {
 // fused-step flags of one launch
 enum : int { kFuseAppend = 1, kOverlapCombine = 2 };
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// Grid-wide "every CTA's KV append is written", in two halves so that only
+// the warp that reads the cache waits.  The count of arrivals only grows (64
+// bits: it does not wrap), so launch n + 1's arrivals take it from
+// (n + 1) * grid to (n + 2) * grid and nothing is reset between launches; a
+// CTA reads its target before it arrives (the count cannot reach the target
+// without it).  Arrival is one release atomic after the CTA's rows are
+// written; the wait polls with acquire loads.  The launch is cooperative, so
+// every CTA is resident and the wait ends; it still gives up after limit_ns.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Bounded grid-wide rendezvous, called by one thread per CTA.  The launch is
-// cooperative, so every CTA is resident and the barrier cannot deadlock; it
-// still gives up after limit_ns (returns false) rather than spin forever.  The
-// generation word only grows, so no reset is needed between launches.
-__device__ __forceinline__ bool grid_barrier(int* ctrl, uint64_t limit_ns) {
-  volatile int* gen_p = ctrl + kGridGenOffset;
-  int* count = ctrl + kGridCountOffset;
-  const int gen = *gen_p;
-  __threadfence();
-  if (atomicAdd(count, 1) == static_cast<int>(gridDim.x) - 1) {
-    atomicExch(count, 0);
-    __threadfence();
-    atomicAdd(ctrl + kGridGenOffset, 1);
-    return true;
-  }
+__device__ __forceinline__ unsigned long long grid_target(int* ctrl) {
+  const unsigned long long g = gridDim.x;
+  return (ld_acquire_u64(reinterpret_cast<const unsigned long long*>(ctrl + kGridCountOffset)) / g + 1) * g;
+}
+
+__device__ __forceinline__ void grid_arrive(int* ctrl) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctrl + kGridCountOffset) : "memory");
+}
+
+__device__ __forceinline__ bool grid_wait(int* ctrl, unsigned long long target, uint64_t limit_ns) {
+  const unsigned long long* c = reinterpret_cast<const unsigned long long*>(ctrl + kGridCountOffset);
+  if (ld_acquire_u64(c) >= target) return true;
   const uint64_t t0 = global_timer_ns();
-  while (*gen_p == gen) {
+  while (ld_acquire_u64(c) < target)
     if (global_timer_ns() - t0 > limit_ns) return false;
-    __nanosleep(64);
-  }
-  __threadfence();
   return true;
 }
 
@@ -572,25 +576,22 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
   __syncthreads();
   const int BZ = B * Z;  // partition-0 units
 
+  // fused step: the count the arrivals of this launch end at, read before this
+  // CTA arrives (only the producer's first lane uses it)
+  unsigned long long grid_target_ = 0;
+  if ((flags & kFuseAppend) && warp == W && lane == 0) grid_target_ = grid_target(p.err);
   // fused step: this CTA's share of the KV append, made visible to the other
-  // CTAs' tensor copies before any of them reads the cache (grid barrier below)
+  // CTAs' tensor copies before any of them reads the cache (the producer
+  // announces this CTA's rows and waits for every other CTA's, below)
   if (flags & kFuseAppend) {
     const int64_t rows = static_cast<int64_t>(ap.num_tokens) * ap.num_kv_heads;
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * (W + 2) + warp; r < rows;
          r += static_cast<int64_t>(gridDim.x) * (W + 2))
       append_row(ap, r, lane);
     asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncthreads();  // this CTA's rows are written; the producer announces them (grid_arrive)
   }
   bool failed = false;  // a bounded wait gave up: skip to the end, still meet every barrier
-  auto cta_grid_sync = [&]() -> bool {
-    named_barrier_sync(2, PS::kThreads);
-    if (threadIdx.x == 0) wsum[8] = grid_barrier(p.err, p.wait_limit_ns) ? 1 : 0;
-    named_barrier_sync(2, PS::kThreads);
-    const bool ok_ = wsum[8] != 0;
-    if (!ok_ && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    return ok_;
-  };
 
   if (warp == W + 1) {
     // ------------------------------- scheduler -------------------------------
@@ -634,13 +635,13 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       const int nblk = p.part_tokens >> p.log2_bs;
       const int j0 = tb >> p.log2_bs;
       const int span = kMaxGroup - (b % kMaxGroup);  // b .. b+span-1 may form b's group
-      auto load_row = [&](int bb, int& v0, int& v1) {
+      auto load_row = [&](int bb, int& v0, int& v1) {  // entries within the table's width only
         v0 = -1;
         v1 = -1;
         if (bb >= 0 && bb < B) {
           const int32_t* r = p.block_tables + static_cast<int64_t>(bb) * p.bt_stride + j0;
-          if (lane < nblk) v0 = r[lane];
-          if (lane + 32 < nblk) v1 = r[lane + 32];
+          if (lane < nblk && j0 + lane < p.max_blocks) v0 = r[lane];
+          if (lane + 32 < nblk && j0 + lane + 32 < p.max_blocks) v1 = r[lane + 32];
         }
       };
       // lane i <= kMaxGroup: whether row b-1+i fills the partition
@@ -712,19 +713,37 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
     // unit u -> (sequence, partition, kv-head tile) and the table entries of
     // its first 32 chunks (two per chunk when blocks hold 8 tokens).  Returns
     // false past the last unit.
+    // prefix groups apply to whole partitions of whole blocks, at most 64 of them
+    const bool groups_on = kGroupOK && p.prefix_groups && (p.part_tokens & (p.block_size - 1)) == 0 &&
+                           (p.part_tokens >> p.log2_bs) <= 64;
     auto decode_unit = [&](int u, UnitInfo& x, int& e0, int& e1) -> bool {
       int L;
+      int grp = -1;  // prefix group, when already found
       if (u < kPhaseAParts * BZ) {
         x.part = u / BZ;
         const int r = u - x.part * BZ;
-        x.b = r / Z;
-        x.z = r - x.b * Z;
+        // sequences in the order 0, 8, 16, ..., 1, 9, 17, ...: prefix groups are
+        // cut at multiples of kMaxGroup, so a launch's first units are group
+        // leaders (real work), and the units that turn out covered come later
+        const int bi = r / Z;
+        int k = 0, base = 0, cnt = (B + kMaxGroup - 1) / kMaxGroup;
+        while (k < kMaxGroup - 1 && bi >= base + cnt) {
+          base += cnt;
+          ++k;
+          cnt = (B - k + kMaxGroup - 1) / kMaxGroup;
+        }
+        x.b = k + kMaxGroup * (bi - base);
+        x.z = r - bi * Z;
         int Lraw = p.context_lens[x.b];  // issued together with the table loads below
         const int32_t* bt_row = p.block_tables + static_cast<int64_t>(x.b) * p.bt_stride;
         x.tb = x.part * p.part_tokens;
         const int j0 = (x.tb + kChunk * lane) >> p.log2_bs;
         int r0 = j0 < p.max_blocks ? bt_row[j0] : 0;
         int r1 = (p.log2_bs < 4 && j0 + 1 < p.max_blocks) ? bt_row[j0 + 1] : 0;
+        // the launch's first units: the neighbours' lengths and tables load
+        // alongside this unit's own (one round trip, not two); the result is
+        // used only if the sequence fills the partition
+        if (groups_on) grp = prefix_group(x.b, x.tb);
         if (Lraw < 0 || Lraw > l_max) {
           if (lane == 0 && x.part == 0) atomicOr(p.err, kErrLen);
           Lraw = Lraw < 0 ? 0 : l_max;
@@ -792,11 +811,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       x.h0 = x.kvh * p.group + (x.z - x.kvh * p.num_head_tiles) * HT;
       x.nh = min(HT, p.group - (x.z - x.kvh * p.num_head_tiles) * HT);
       x.group = 1;
-      if constexpr (kGroupOK) {
-        if (p.prefix_groups && L >= x.tb + p.part_tokens && (p.part_tokens & (p.block_size - 1)) == 0 &&
-            (p.part_tokens >> p.log2_bs) <= 64)
-          x.group = prefix_group(x.b, x.tb);
-      }
+      if (groups_on && L >= x.tb + p.part_tokens) x.group = grp >= 0 ? grp : prefix_group(x.b, x.tb);
       return true;
     };
     // Finished units of split sequences (the consumers' done ring): each is
@@ -888,9 +903,6 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
     UnitInfo cur{};
     int e0 = 0, e1 = 0;
     bool have_cur = decode_unit(static_cast<int>(blockIdx.x), cur, e0, e1);
-    if (flags & kFuseAppend) {
-      if (!cta_grid_sync()) ok = false;
-    }
     while (ok && have_cur) {
       // work estimates: a stage, plus one for the unit merge; stages of a
       // prefix group carry several sequences
@@ -956,7 +968,14 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       tma_prefetch_desc(&vmap);
     }
     if (flags & kFuseAppend) {  // no cache read before every CTA's append is done
-      if (!cta_grid_sync()) failed = true;
+      grid_arrive(p.err);  // this CTA's rows (the __syncthreads after the append ordered them)
+      bool got = true;
+      if (lane == 0) got = grid_wait(p.err, grid_target_, p.wait_limit_ns);
+      if (__shfl_sync(kFullMask, got ? 1 : 0, 0) == 0) {
+        failed = true;
+        if (lane == 0) atomicOr(p.err, kErrWaitTimeout);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // the other CTAs' rows, for the tensor copies
     }
     int k = 0;   // stage sequence number
     int pk = 0;  // pieces taken
@@ -1123,7 +1142,6 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
     asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory");
     if (threadIdx.x == 0) mbar_arrive(smem_u32(pbar));
   }
-  if ((flags & kFuseAppend) && !cta_grid_sync()) failed = true;
   MmaState<MT, D, NT> st;
   const int cw = warp;
   const uint32_t sync_bar = smem_u32(cbar);

@@ -13,14 +13,13 @@ namespace wllm {
 // The 256-byte per-device control block, offsets in ints: the error word;
 // two spare words used only by the bounded-wait self-test (a counter that
 // stays zero, and its result); the persistent scheduler's claim and finish
-// counters; the fused step's grid-barrier count and generation.
+// counters; the fused step's 64-bit count of CTAs whose KV append is written.
 constexpr int kCtrlBytes = 256;
 constexpr int kSelftestNeverOffset = 8;
 constexpr int kSelftestResultOffset = 9;
 constexpr int kSchedNextOffset = 16;
 constexpr int kSchedDoneOffset = 32;
-constexpr int kGridCountOffset = 48;
-constexpr int kGridGenOffset = 56;
+constexpr int kGridCountOffset = 48;  // 8-byte aligned: two ints
 
 // Kernel launches the library has issued (successful launch calls), for
 // wllm_launch_count().  Every launch site calls note_launch() once per kernel.

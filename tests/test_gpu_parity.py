@@ -498,18 +498,21 @@ def test_split_merge_head_dims(monkeypatch, D, Hq, Hkv, dtype):
     assert torch.equal(int_view(got), int_view(got2))
 
 
-@pytest.mark.parametrize("mode", ["WLLM_SEPARATE_COMBINE"])
-def test_other_combine_modes(monkeypatch, mode):
-    """Split partitions merged by a second kernel instead of inside the launch."""
-    monkeypatch.setenv(mode, "1")
+@pytest.mark.parametrize("value", ["1", "0"])
+def test_other_combine_modes(monkeypatch, value):
+    """Split partitions merged by a second kernel (=1) or inside the launch
+    (=0), forced against the default for the batch size."""
+    monkeypatch.setenv("WLLM_SEPARATE_COMBINE", value)
     monkeypatch.setenv("WLLM_PARTITION_TOKENS", "128")
-    case = workloads.custom_case("sep", lens=[5, 900, 2500, 1], num_q_heads=8, num_kv_heads=2,
+    lens = [5, 900, 2500, 1] if value == "1" else [5, 900, 2500, 1] * 160  # 640 x 8 rows: above the switch
+    case = workloads.custom_case("sep", lens=lens, num_q_heads=8, num_kv_heads=2,
                                  head_dim=64, block_size=16, dtype=torch.float16, seed=44)
     got, _, _ = gpu_step(case)
     ref, _, _ = oracle_step(case)
-    assert_attention_close(got, ref, case.dtype, mode)
+    what = f"WLLM_SEPARATE_COMBINE={value}"
+    assert_attention_close(got, ref, case.dtype, what)
     got2, _, _ = fused_step(case)
-    assert_attention_close(got2, ref, case.dtype, mode + ", step")
+    assert_attention_close(got2, ref, case.dtype, what + ", step")
 
 
 def test_fused_step_without_tokens_or_sequences():

@@ -93,9 +93,12 @@ enum : int { kFirst = 1, kLast = 2, kEmptySeq = 4, kStop = 8, kGroup = 16 };
 // kMaxGroup sequences: the K/V bytes are read once for all of them.
 constexpr int kMaxGroup = 8;
 
-// Unit order.  Phase A: partitions below kPhaseAParts, partition-major in
-// sequence order (decoded without a schedule, and a shared prompt prefix --
-// the first partitions -- is handed out early).  Phase B: the later
+// Unit order.  Phase A: partitions below kPhaseAParts, decoded without a
+// schedule: partition 0 of the sequences at multiples of kMaxGroup (the
+// possible leaders of prefix groups, so a shared prompt prefix is handed out
+// first), then partition 1 of every sequence, then partition 0 of the rest
+// (units a group leader may cover: claimed while earlier work runs, so no CTA
+// starts the launch skipping covered units).  Phase B: the later
 // partitions except each sequence's last, sequence-major (prefix sums).
 // Phase C: each sequence's last partition when it lies beyond phase A,
 // longest first (32 length buckets, ties in sequence order), so the units
@@ -720,11 +723,20 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       int L;
       int grp = -1;  // prefix group, when already found
       if (u < kPhaseAParts * BZ) {
-        x.part = u / BZ;
-        const int r = u - x.part * BZ;
-        // sequences in the order 0, 8, 16, ..., 1, 9, 17, ...: prefix groups are
-        // cut at multiples of kMaxGroup, so a launch's first units are group
-        // leaders (real work), and the units that turn out covered come later
+        static_assert(kPhaseAParts == 2, "phase A is partitions 0 and 1");
+        // sequences in the order 0, 8, 16, ..., 1, 9, 17, ... (prefix groups are
+        // cut at multiples of kMaxGroup): units [0, n0 Z) are partition 0 of
+        // the first n0 of that order, [n0 Z, n0 Z + BZ) partition 1 of all,
+        // the rest partition 0 of the others
+        const int n0Z = (B + kMaxGroup - 1) / kMaxGroup * Z;
+        int r = u;
+        x.part = 0;
+        if (u >= n0Z + BZ) {
+          r = u - BZ;
+        } else if (u >= n0Z) {
+          x.part = 1;
+          r = u - n0Z;
+        }
         const int bi = r / Z;
         int k = 0, base = 0, cnt = (B + kMaxGroup - 1) / kMaxGroup;
         while (k < kMaxGroup - 1 && bi >= base + cnt) {
@@ -1019,25 +1031,20 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
         const int n_stages = (piece_chunks + SUB - 1) / SUB;
         for (int sg = 0; sg < n_stages; ++sg) {
           const int c0 = pc0 + sg * SUB;
-          int pbs0[SUB], pbs1[SUB];
-#pragma unroll
-          for (int j = 0; j < SUB; ++j) {
-            pbs0[j] = __shfl_sync(kFullMask, e0, (sg * SUB + j) & 31);
-            pbs1[j] = __shfl_sync(kFullMask, e1, (sg * SUB + j) & 31);
-          }
           if (!acquire_stage(k)) { ok = false; break; }
+          const int s = k % S;
+          const int t0 = cur.tb + kChunk * c0;
+          const int nsub = min(SUB, cur.n_chunks - c0);
+          const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
+          const uint32_t bar = smem_u32(full + s);
+          const bool first = (pflags & kPieceFirst) && sg == 0;
+          const bool two = p.log2_bs < 4;  // 8-token blocks: two 8-row boxes per 16-token sub-chunk
+          const bool q_rows = first && cur.group == 1;  // group units read q from global memory
           if (lane == 0) {
-            const int s = k % S;
-            const int t0 = cur.tb + kChunk * c0;
-            const int nsub = min(SUB, cur.n_chunks - c0);
-            const uint32_t stage = smem_u32(ring + s * PS::kStageBytes);
-            const uint32_t bar = smem_u32(full + s);
-            const bool first = (pflags & kPieceFirst) && sg == 0;
             const int flags = (first ? kFirst : 0) | ((pflags & kPieceLast) && sg == n_stages - 1 ? kLast : 0) |
                               (cur.group > 1 ? kGroup : 0);
             meta[s] = StageMeta{cur.b, cur.part, t0, cur.te, cur.n_parts, cur.h0, cur.nh, flags, cur.z, nsub,
                                 cur.group, 0};
-            const bool two = p.log2_bs < 4;
             uint32_t bytes = 0;
 #pragma unroll
             for (int j = 0; j < SUB; ++j) {
@@ -1046,46 +1053,45 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
                 bytes += (two && !(tj + 8 < cur.te)) ? G::kStageBytes / 2 : G::kStageBytes;
               }
             }
-            const bool q_rows = first && cur.group == 1;  // group units read q from global memory
             if (q_rows) bytes += cur.nh * D * static_cast<int>(sizeof(T));
             mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-            for (int j = 0; j < SUB; ++j) {
-              if (j < nsub) {
-                const int tj = t0 + kChunk * j;
-                const uint32_t kdst = stage + j * PS::kKV;
-                const uint32_t vdst = stage + (SUB + j) * PS::kKV;
-                if constexpr (G::kPairRows) {  // rows of two tokens; blocks of >= 16 tokens (host-checked)
-                  const int y = (cur.kvh * p.block_size + (tj & (p.block_size - 1))) >> 1;
-                  tma_load_3d(kdst, &kmap, bar, 0, y, pbs0[j]);
-                  tma_load_3d(vdst, &vmap, bar, 0, y, pbs0[j]);
-                } else if (!two) {
-                  const int y = cur.kvh * p.block_size + (tj & (p.block_size - 1));
-#pragma unroll
-                  for (int cb = 0; cb < G::kColBoxes; ++cb) {
-                    tma_load_3d(kdst + cb * 2048, &kmap, bar, cb * G::kBoxCols, y, pbs0[j]);
-                    tma_load_3d(vdst + cb * 2048, &vmap, bar, cb * G::kBoxCols, y, pbs0[j]);
-                  }
-                } else {
-                  const int y = cur.kvh * p.block_size;
-                  const bool has1 = tj + 8 < cur.te;
-#pragma unroll
-                  for (int cb = 0; cb < G::kColBoxes; ++cb) {
-                    tma_load_3d(kdst + cb * 2048, &kmap, bar, cb * G::kBoxCols, y, pbs0[j]);
-                    tma_load_3d(vdst + cb * 2048, &vmap, bar, cb * G::kBoxCols, y, pbs0[j]);
-                    if (has1) {
-                      tma_load_3d(kdst + cb * 2048 + 1024, &kmap, bar, cb * G::kBoxCols, y, pbs1[j]);
-                      tma_load_3d(vdst + cb * 2048 + 1024, &vmap, bar, cb * G::kBoxCols, y, pbs1[j]);
-                    }
-                  }
-                }
+          }
+          __syncwarp();
+          // the stage's tensor copies, one per lane (issued from one lane they
+          // take about a microsecond per stage, which bounds a CTA's stream):
+          // copy i is box cb (and, with 8-token blocks, 8-row half `half`) of
+          // the K (kv = 0) or V tile of sub-chunk j,
+          // i = ((j * 2 + kv) * kColBoxes + cb) * H + half
+          const int H = (!G::kPairRows && two) ? 2 : 1;
+          const int n_copies = nsub * 2 * G::kColBoxes * H;
+          for (int base = 0; base < n_copies; base += 32) {
+            const int i = base + lane;
+            int r = i < n_copies ? i : 0;
+            const int half = r % H;
+            r /= H;
+            const int cb = r % G::kColBoxes;
+            r /= G::kColBoxes;
+            const int kv = r & 1, j = r >> 1;
+            const int src = (sg * SUB + j) & 31;
+            const int blk0 = __shfl_sync(kFullMask, e0, src), blk1 = __shfl_sync(kFullMask, e1, src);
+            const int tj = t0 + kChunk * j;
+            if (i < n_copies && !(half == 1 && !(tj + 8 < cur.te))) {
+              const uint32_t dst = stage + (kv * SUB + j) * PS::kKV + cb * 2048 + half * 1024;
+              const CUtensorMap* map = kv ? &vmap : &kmap;
+              if constexpr (G::kPairRows) {  // rows of two tokens; blocks of >= 16 tokens (host-checked)
+                tma_load_3d(dst, map, bar, 0, (cur.kvh * p.block_size + (tj & (p.block_size - 1))) >> 1, blk0);
+              } else if (!two) {
+                tma_load_3d(dst, map, bar, cb * G::kBoxCols, cur.kvh * p.block_size + (tj & (p.block_size - 1)),
+                            blk0);
+              } else {
+                tma_load_3d(dst, map, bar, cb * G::kBoxCols, cur.kvh * p.block_size, half ? blk1 : blk0);
               }
             }
-            if (q_rows) {
-              for (int hh = 0; hh < cur.nh; ++hh)
-                bulk_load(stage + 2 * SUB * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
-                          D * static_cast<int>(sizeof(T)), bar);
-            }
+          }
+          if (q_rows) {
+            for (int hh = lane; hh < cur.nh; hh += 32)
+              bulk_load(stage + 2 * SUB * PS::kKV + hh * D * static_cast<int>(sizeof(T)), qsrc + hh * p.q_sh,
+                        D * static_cast<int>(sizeof(T)), bar);
           }
           ++k;
         }

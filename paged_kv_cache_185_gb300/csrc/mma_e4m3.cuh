@@ -131,7 +131,9 @@ __device__ __forceinline__ void mma_chunks_e4m3(MmaState<__half, D, NT>& st, uin
     }
   }
 
-  // online softmax over the NS sub-chunks (this lane: tokens lane/4 and lane/4 + 8 of each)
+  // online softmax over the NS sub-chunks (this lane: tokens lane/4 and lane/4 + 8 of each);
+  // a step wholly inside the context needs no mask
+  const bool full = t0 + NS * kChunk <= tok_end;
   float alpha[NT][2];
   uint32_t pb[NS][NT][2];
   bool rescale = false;
@@ -141,7 +143,7 @@ __device__ __forceinline__ void mma_chunks_e4m3(MmaState<__half, D, NT>& st, uin
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
       const int tok_a = t0 + j * kChunk + (lane >> 2);
-      const bool va = tok_a < tok_end, vb = tok_a + 8 < tok_end;
+      const bool va = full || tok_a < tok_end, vb = full || tok_a + 8 < tok_end;
       s[j][nt][0] = va ? s[j][nt][0] * scale_log2 : -INFINITY;
       s[j][nt][1] = va ? s[j][nt][1] * scale_log2 : -INFINITY;
       s[j][nt][2] = vb ? s[j][nt][2] * scale_log2 : -INFINITY;
@@ -161,9 +163,9 @@ __device__ __forceinline__ void mma_chunks_e4m3(MmaState<__half, D, NT>& st, uin
     st.m[nt][1] = mn1;
     float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < NS; ++j) {
-      const float p0 = exp2f(s[j][nt][0] - mn0), p1 = exp2f(s[j][nt][1] - mn1);
-      const float p2 = exp2f(s[j][nt][2] - mn0), p3 = exp2f(s[j][nt][3] - mn1);
+    for (int j = 0; j < NS; ++j) {  // one SFU exponential each: the weights are rounded to f16 next
+      const float p0 = ex2_approx(s[j][nt][0] - mn0), p1 = ex2_approx(s[j][nt][1] - mn1);
+      const float p2 = ex2_approx(s[j][nt][2] - mn0), p3 = ex2_approx(s[j][nt][3] - mn1);
       l0 += p0 + p2;
       l1 += p1 + p3;
       pb[j][nt][0] = movmatrix_trans(Mma<__half>::pack(p0, p1));

@@ -647,15 +647,27 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
           if (lane + 32 < nblk && j0 + lane + 32 < p.max_blocks) v1 = r[lane + 32];
         }
       };
-      // lane i <= kMaxGroup: whether row b-1+i fills the partition
+      // lane i <= kMaxGroup: whether row b-1+i fills the partition, and the
+      // partition's first block in that row (one round trip for both)
       const int bb_l = b - 1 + lane;
       bool cov = false;
+      int first = -1;
       if (lane <= kMaxGroup && bb_l >= 0 && bb_l < B) {
         int Lb = p.context_lens[bb_l];
+        if (j0 < p.max_blocks) first = p.block_tables[static_cast<int64_t>(bb_l) * p.bt_stride + j0];
         Lb = Lb < 0 ? 0 : (Lb > l_max ? l_max : Lb);
         cov = Lb >= tb + p.part_tokens;
       }
       const unsigned covm = __ballot_sync(kFullMask, cov);
+      // rows whose first block differs cannot share the partition: when no
+      // neighbour that could join (b-1 as b's leader, b+1 as its first
+      // follower) starts with b's block, there is no group and no table is
+      // compared
+      const int b_first = __shfl_sync(kFullMask, first, 1);
+      const unsigned cand = __ballot_sync(kFullMask, cov && first == b_first) & covm;
+      const bool lead_cand = b % kMaxGroup != 0 && b > 0 && (cand & 1u);
+      const bool next_cand = span >= 2 && ((cand >> 2) & 1u);
+      if (!lead_cand && !next_cand) return 1;
       int r0[kMaxGroup + 1], r1[kMaxGroup + 1];  // rows b-1 .. b+kMaxGroup-1
 #pragma unroll
       for (int i = 0; i <= kMaxGroup; ++i) {
@@ -810,6 +822,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
           const int r = u2 - prefix[lo];
           x.part = kPhaseAParts + r / Z;
           x.z = r - (r / Z) * Z;
+          // (a phase-B partition is never a sequence's last, so it is full)
+          if (groups_on) grp = prefix_group(x.b, x.part * p.part_tokens);
           L = p.context_lens[lo];  // checked and clamped by the consumers' prefix pass
           L = L < 0 ? 0 : (L > l_max ? l_max : L);
           x.tb = x.part * p.part_tokens;

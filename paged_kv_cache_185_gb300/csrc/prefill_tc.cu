@@ -11,7 +11,9 @@
 // One CTA (one per SM) owns 256 query rows of one sequence and one kv head,
 // as two 128-row tiles -- row r of the sequence's chunk is (token r / G, query
 // head r % G of the kv head's group), so the G heads of a group and both tiles
-// share every staged K/V byte -- and walks the rows' context in 128-token kv
+// share every staged K/V byte.  CTAs are launched longest context first (the
+// kv heads of a row block together), so that the short ones fill the end of
+// the launch.  A CTA walks the rows' context in 128-token kv
 // tiles.  Tensor memory holds, per Q tile, the scores S (128 columns, fp32),
 // over which the softmax writes the weights P (16-bit, two per column), and the
 // output O (head_dim columns).  Ten warps:
@@ -62,6 +64,7 @@ constexpr int kTcRows = kTcTileRows * kTcTiles;       // query rows per CTA
 constexpr int kTcKv = 128;                            // kv tokens per kv tile
 constexpr int kTcThreads = (2 + 4 * kTcTiles) * 32;   // producer, MMA, four softmax warps per Q tile
 constexpr float kTcRescale = 8.f;                     // the running maximum moves by more than 8 (log2) only
+constexpr int kTcSortSeqs = 64;                       // batches of up to this many sequences: longest first
 
 template <int D>
 struct TcShape {
@@ -150,13 +153,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int kvh = blockIdx.y;
+  // CTA i works on kv head i % Hkv of row block i / Hkv: the kv heads of a
+  // row block are launched together
+  const int kvh = static_cast<int>(blockIdx.x % p.num_kv_heads);
+  const int tgt_block = static_cast<int>(blockIdx.x / p.num_kv_heads);
 
   // ---- which (sequence, row block) this CTA owns: sequence b owns
-  // ceil(n_b * G / 256) consecutive slots of blockIdx.x
+  // ceil(n_b * G / 256) consecutive row blocks.  With up to kTcSortSeqs
+  // sequences they are taken longest context first (the block scheduler
+  // starts CTAs in launch order, so the longest CTAs start first and the
+  // short ones fill the end); within a sequence its last rows (the longest
+  // context) come first.
   if (warp == 0) {
     int seq = -1, tile = 0, base = 0;
-    for (int b0 = 0; b0 < p.num_seqs && seq < 0; b0 += 32) {
+    if (p.num_seqs <= kTcSortSeqs) {
+      // lane l holds sequences l and l + 32: length (the sort key) and row blocks
+      int key[2], nb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = lane + 32 * h;
+        key[h] = -1;
+        nb[h] = 0;
+        if (b < p.num_seqs) {
+          int n = p.query_start_loc[b + 1] - p.query_start_loc[b];
+          n = n < 0 ? 0 : n;
+          nb[h] = static_cast<int>((static_cast<int64_t>(n) * G + kTcRows - 1) / kTcRows);
+          key[h] = p.context_lens[b];
+        }
+      }
+      // start of each of this lane's sequences in the sorted order (ties in sequence order)
+      int start[2] = {0, 0};
+      for (int bb = 0; bb < p.num_seqs; ++bb) {
+        const int kb = __shfl_sync(kFullMask, bb < 32 ? key[0] : key[1], bb & 31);
+        const int nbb = __shfl_sync(kFullMask, bb < 32 ? nb[0] : nb[1], bb & 31);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int b = lane + 32 * h;
+          if (kb > key[h] || (kb == key[h] && bb < b)) start[h] += nbb;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = lane + 32 * h;
+        const bool hit = b < p.num_seqs && tgt_block >= start[h] && tgt_block < start[h] + nb[h];
+        const unsigned m = __ballot_sync(kFullMask, hit);
+        if (m != 0u) {
+          const int src = __ffs(m) - 1;
+          seq = src + 32 * h;
+          tile = __shfl_sync(kFullMask, nb[h] - 1 - (tgt_block - start[h]), src);
+        }
+      }
+    }
+    for (int b0 = 0; b0 < p.num_seqs && seq < 0 && p.num_seqs > kTcSortSeqs; b0 += 32) {
       const int b = b0 + lane;
       int n = 0;
       if (b < p.num_seqs) n = p.query_start_loc[b + 1] - p.query_start_loc[b];
@@ -169,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane >= off) incl += v;
       }
       const int excl = incl - tiles;
-      const int tgt = static_cast<int>(blockIdx.x) - base;
+      const int tgt = tgt_block - base;
       const unsigned hit = __ballot_sync(kFullMask, b < p.num_seqs && tgt >= excl && tgt < incl);
       if (hit != 0u) {
         const int src = __ffs(hit) - 1;
@@ -544,7 +592,8 @@ int launch_tc_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, const Prefi
   cudaError_t e =
       static_cast<cudaError_t>(raise_smem_limit(configured_for, reinterpret_cast<const void*>(kernel), TS::kSmem));
   if (e != cudaSuccess) return e;
-  kernel<<<dim3(grid_x, p.num_kv_heads), kTcThreads, TS::kSmem, stream>>>(kmap, vmap, p);
+  kernel<<<static_cast<unsigned>(grid_x) * static_cast<unsigned>(p.num_kv_heads), kTcThreads, TS::kSmem, stream>>>(
+      kmap, vmap, p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;

@@ -558,6 +558,9 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
   const int B = p.num_seqs;
   const int Z = p.num_kv_heads * p.num_head_tiles;
   const int l_max = p.max_blocks * p.block_size;
+  // a separate merge kernel launched behind this one may be scheduled now: its
+  // CTAs take the SMs as this grid's CTAs leave, and wait for the whole grid
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1471,8 +1474,12 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
 
 // Combine kernel for launches that split sequences into partitions: one warp
 // per query row.
+// Launched as a programmatic dependent of the decode: its CTAs may start
+// while the decode's last CTAs still run, and wait here until the decode grid
+// has completed and its partials are visible.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) splitkv_combine(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= p.num_seqs * p.num_q_heads) return;
   const int rows[1] = {row};
@@ -1530,8 +1537,20 @@ int launch_persistent_inst(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     note_launch();
   }
   if (!separate_combine || fuse_combine) return cudaSuccess;
-  splitkv_combine<T, D><<<(p.num_seqs * p.num_q_heads + 7) / 8, 256, 0, stream>>>(p);
-  e = cudaGetLastError();
+  // programmatic dependent launch: no launch gap between the decode's last
+  // CTAs and the merge (the merge's griddepcontrol.wait orders its reads)
+  cudaLaunchConfig_t ccfg{};
+  ccfg.gridDim = dim3((p.num_seqs * p.num_q_heads + 7) / 8);
+  ccfg.blockDim = dim3(256);
+  ccfg.dynamicSmemBytes = 0;
+  ccfg.stream = stream;
+  cudaLaunchAttribute cattr[1];
+  cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  cattr[0].val.programmaticStreamSerializationAllowed = 1;
+  ccfg.attrs = cattr;
+  ccfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&ccfg, splitkv_combine<T, D>, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }

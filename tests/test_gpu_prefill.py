@@ -73,6 +73,19 @@ def test_prefill_matches_oracle(Hq, Hkv, D, bs, lens, chunks, dtype, kernel):
     assert_attention_close(got, ref, dtype, f"prefill {Hq}/{Hkv} D{D} bs{bs}")
 
 
+@pytest.mark.parametrize("nseq", [64, 70])
+def test_prefill_many_sequences_in_either_launch_order(nseq, kernel):
+    """Up to 64 sequences the tcgen05 kernel launches its CTAs longest context
+    first (equal lengths in sequence order); above 64, in sequence order: every
+    row block is covered exactly once either way."""
+    rng = np.random.default_rng(nseq)
+    lens = rng.integers(1, 400, size=nseq)
+    lens[::5] = 300  # ties in the ranking
+    chunks = np.minimum(lens, rng.integers(0, 40, size=nseq))
+    case, q, qsl = prefill_case(lens, chunks, 16, 4, 64, 16, torch.float16, seed=nseq + 3)
+    assert_attention_close(run_gpu(case, q, qsl), run_oracle(case, q, qsl), torch.float16, f"{nseq} sequences")
+
+
 def test_prefill_one_token_chunks_match_decode(kernel):
     # n_b = 1 everywhere: the decode's answer
     rng = np.random.default_rng(2)

@@ -586,16 +586,19 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
   // CTA arrives (only the producer's first lane uses it)
   unsigned long long grid_target_ = 0;
   if ((flags & kFuseAppend) && warp == W && lane == 0) grid_target_ = grid_target(p.err);
-  // fused step: this CTA's share of the KV append, made visible to the other
-  // CTAs' tensor copies before any of them reads the cache (the producer
-  // announces this CTA's rows and waits for every other CTA's, below)
-  if (flags & kFuseAppend) {
+  // fused step: this CTA's share of the KV append (consumer and producer
+  // warps), made visible to the other CTAs' tensor copies before any of them
+  // reads the cache (the producer announces this CTA's rows and waits for
+  // every other CTA's, below).  The scheduler warp does not take part: it
+  // decodes its first units meanwhile (only tensor copies read the cache).
+  if ((flags & kFuseAppend) && warp <= W) {
     const int64_t rows = static_cast<int64_t>(ap.num_tokens) * ap.num_kv_heads;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (W + 2) + warp; r < rows;
-         r += static_cast<int64_t>(gridDim.x) * (W + 2))
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (W + 1) + warp; r < rows;
+         r += static_cast<int64_t>(gridDim.x) * (W + 1))
       append_row(ap, r, lane);
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    __syncthreads();  // this CTA's rows are written; the producer announces them (grid_arrive)
+    // this CTA's rows are written; the producer announces them (grid_arrive)
+    asm volatile("bar.sync 2, %0;" ::"r"((W + 1) * 32) : "memory");
   }
   bool failed = false;  // a bounded wait gave up: skip to the end, still meet every barrier
 

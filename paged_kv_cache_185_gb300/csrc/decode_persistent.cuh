@@ -51,25 +51,36 @@ enum : int { kFuseAppend = 1, kOverlapCombine = 2 };
 
 // Grid-wide "every CTA's KV append is written", in two halves so that only
 // the warp that reads the cache waits.  The count of arrivals only grows (64
-// bits: it does not wrap), so launch n + 1's arrivals take it from
-// (n + 1) * grid to (n + 2) * grid and nothing is reset between launches; a
-// CTA reads its target before it arrives (the count cannot reach the target
-// without it).  Arrival is one release atomic after the CTA's rows are
-// written; the wait polls with acquire loads.  The launch is cooperative, so
-// every CTA is resident and the wait ends; it still gives up after limit_ns.
+// bits: it does not wrap) and is never reset: every launch adds exactly
+// kGridWeight in total, CTA i of g adding
+// floor(kGridWeight (i+1) / g) - floor(kGridWeight i / g) (at least 1), so the
+// count is a multiple of kGridWeight between launches whatever their grid
+// sizes, and a launch's barrier opens at the next multiple.  A CTA reads its
+// target (a relaxed load: only the value matters) before it arrives, so the
+// count cannot reach the target without it.  Arrival is one release
+// reduction by one thread, after the CTA's rows are written and ordered
+// before it; the wait polls with acquire loads.  The launch is cooperative,
+// so every CTA is resident and the wait ends; it still gives up after
+// limit_ns.
+constexpr unsigned long long kGridWeight = 1ull << 20;  // > any grid size
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ unsigned long long grid_target(int* ctrl) {
-  const unsigned long long g = gridDim.x;
-  return (ld_acquire_u64(reinterpret_cast<const unsigned long long*>(ctrl + kGridCountOffset)) / g + 1) * g;
+__device__ __forceinline__ unsigned long long grid_target(const int* ctrl) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctrl + kGridCountOffset));
+  return (v / kGridWeight + 1) * kGridWeight;
 }
 
+// one thread per CTA
 __device__ __forceinline__ void grid_arrive(int* ctrl) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctrl + kGridCountOffset) : "memory");
+  const unsigned long long g = gridDim.x, i = blockIdx.x;
+  const unsigned long long w = kGridWeight * (i + 1) / g - kGridWeight * i / g;
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ctrl + kGridCountOffset), "l"(w) : "memory");
 }
 
 __device__ __forceinline__ bool grid_wait(int* ctrl, unsigned long long target, uint64_t limit_ns) {
@@ -1000,7 +1011,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       tma_prefetch_desc(&vmap);
     }
     if (flags & kFuseAppend) {  // no cache read before every CTA's append is done
-      grid_arrive(p.err);  // this CTA's rows (the __syncthreads after the append ordered them)
+      if (lane == 0) grid_arrive(p.err);  // this CTA's rows (ordered by the bar.sync after the append)
       bool got = true;
       if (lane == 0) got = grid_wait(p.err, grid_target_, p.wait_limit_ns);
       if (__shfl_sync(kFullMask, got ? 1 : 0, 0) == 0) {

@@ -515,6 +515,27 @@ def test_other_combine_modes(monkeypatch, value):
     assert_attention_close(got2, ref, case.dtype, what + ", step")
 
 
+def test_fused_steps_of_different_grid_sizes():
+    """Fused steps whose launches have very different grids (4 CTAs, then a
+    full persistent grid), alternated on one device: the grid barrier's count
+    stays consistent across grid sizes, so every step appends bit for bit and
+    decodes against the oracle, with no error reported."""
+    small = workloads.custom_case("grid_small", lens=[40, 17], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                                  block_size=16, dtype=torch.bfloat16, seed=46)
+    rng = np.random.default_rng(47)
+    big = workloads.custom_case("grid_big", lens=rng.integers(300, 1200, 64).tolist(), num_q_heads=32,
+                                num_kv_heads=4, head_dim=64, block_size=16, dtype=torch.float16, seed=48)
+    refs = {c.name: oracle_step(c) for c in (small, big)}
+    assert wllm.device_errors() == 0
+    for case in (small, big, small, big, big, small, big):
+        got, kc, vc = fused_step(case)
+        ref, kr, vr = refs[case.name]
+        assert torch.equal(int_view(kc.cpu()), int_view(kr)), f"{case.name}: K append not bit-exact"
+        assert torch.equal(int_view(vc.cpu()), int_view(vr)), f"{case.name}: V append not bit-exact"
+        assert_attention_close(got, ref, case.dtype, f"{case.name} after a launch of another grid size")
+        assert wllm.device_errors() == 0
+
+
 def test_fused_step_without_tokens_or_sequences():
     case = workloads.custom_case("noapp", lens=[40, 17], num_q_heads=4, num_kv_heads=2, head_dim=64,
                                  block_size=16, dtype=torch.bfloat16, seed=45, append="none")

@@ -135,8 +135,13 @@ struct UnitInfo {
 constexpr int kPieceChunks = 32;
 constexpr int kQueue = 4;  // pieces in flight between scheduler and producer
 // The scheduler claims another unit only when at most this much work (in
-// 64-token stage equivalents) waits in its queue.
-constexpr int kLookahead = 8;
+// stage equivalents) waits in its queue: little when the launch has few units
+// per CTA (the finish balances better), more when it has many (a claim and
+// its decode take a few microseconds of dependent round trips, which a short
+// unit does not cover).  Measured on GB300 against one bound of 8 for all:
+// TinyLlama-shaped step 33.7 -> 32.1 us, Qwen2.5 prefix 176.8 -> 174.4 us,
+// its fp8 step 128.7 -> 126.1 us, long-context step unchanged.
+constexpr int kLookaheadFew = 4, kLookaheadMany = 12;
 enum : int { kPieceFirst = 1, kPieceLast = 2, kPieceStop = 4 };
 struct Piece {
   UnitInfo u;
@@ -914,6 +919,8 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       }
     };
     bool ok = true;
+    // phase A alone has 2 B Z units: fewer than 4 per CTA is a launch of few units
+    const int lookahead = 2 * BZ < 4 * static_cast<int>(gridDim.x) ? kLookaheadFew : kLookaheadMany;
     int pk = 0;        // pieces handed over
     int taken = 0;     // pieces the producer is known to have taken
     int queued = 0;    // work handed over but not yet taken, in stage equivalents
@@ -967,7 +974,7 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
       service();
       // claim the next unit only when little work is left queued, so that at
       // the end no CTA sits on claimed units while others run dry
-      while (ok && taken < pk && queued > kLookahead) ok = retire();
+      while (ok && taken < pk && queued > lookahead) ok = retire();
       if (!ok) break;
       int u_nxt = 0;
       if (lane == 0) u_nxt = static_cast<int>(gridDim.x) + atomicAdd(sched_next, 1);

@@ -171,6 +171,47 @@ def test_fp8_decode_step_fused(dtype):
     assert_attention_close(out.to(dev).cpu(), ref, dtype, "fused fp8 step")
 
 
+def test_fp8_fused_steps_of_different_grid_sizes():
+    """fp8 fused steps whose launches have very different grids (2 CTAs, then
+    a full persistent grid), alternated with a 16-bit one on the same device:
+    the grid barrier stays consistent, every step's append is bit-exact and
+    its decode matches the oracle, with no error reported."""
+    ks, vs = 0.23, 0.29
+    small = custom_case("fp8_grid_small", lens=[37, 16], num_q_heads=8, num_kv_heads=1, head_dim=128,
+                        block_size=16, dtype=torch.bfloat16, seed=61, append="tail")
+    rng = np.random.default_rng(62)
+    big = custom_case("fp8_grid_big", lens=rng.integers(200, 3000, 96).tolist(), num_q_heads=28, num_kv_heads=4,
+                      head_dim=128, block_size=16, dtype=torch.bfloat16, seed=63, append="tail")
+    refs = {}
+    for c in (small, big):
+        kc, vc = fp8_pools(c)
+        oracle.reshape_and_cache_e4m3(c.key, c.value, kc, vc, c.slot_mapping, ks, vs)
+        refs[c.name] = (kc, vc, oracle_decode_fp8(c, kc, vc, ks, vs))
+    b16 = custom_case("b16_grid", lens=[5, 900], num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                      dtype=torch.float16, seed=64)
+    assert wllm.device_errors() == 0
+    for case in (small, big, b16, small, big, big, small):
+        q = case.q.cuda()
+        out = torch.empty_like(q)
+        if case is b16:
+            kd, vd = case.pool("cuda")
+            wllm.decode_step(out, q, case.key.cuda(), case.value.cuda(), kd, vd, case.slot_mapping.cuda(),
+                             case.block_tables.cuda(), case.context_lens.cuda(), case.num_kv_heads, case.scale,
+                             case.block_size)
+            torch.cuda.synchronize()
+            assert wllm.device_errors() == 0
+            continue
+        kd, vd = (x.cuda() for x in fp8_pools(case))
+        wllm.decode_step_fp8(out, q, case.key.cuda(), case.value.cuda(), kd, vd, case.slot_mapping.cuda(),
+                             case.block_tables.cuda(), case.context_lens.cuda(), case.num_kv_heads, case.scale, ks,
+                             vs, case.block_size)
+        torch.cuda.synchronize()
+        kr, vr, ref = refs[case.name]
+        assert torch.equal(kd.cpu(), kr) and torch.equal(vd.cpu(), vr), f"{case.name}: append not bit-exact"
+        assert_attention_close(out.cpu(), ref, case.dtype, f"{case.name} after a launch of another grid size")
+        assert wllm.device_errors() == 0
+
+
 def test_fp8_rejects_unsupported_shapes():
     case = custom_case("fp8_d64", lens=[10], num_q_heads=4, num_kv_heads=2, head_dim=64, block_size=8,
                        dtype=torch.float16, seed=1, append="none")

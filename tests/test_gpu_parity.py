@@ -419,6 +419,24 @@ def test_large_batch_is_sliced():
     assert_attention_close(got, ref, case.dtype, "4300 sequences")
 
 
+def test_large_batch_fused_step_with_splits(monkeypatch):
+    """A fused step over more sequences than one launch takes, split into
+    partitions: the first slice's launch appends every sequence's rows, the
+    later slices decode after it, each slice merges its split rows."""
+    monkeypatch.setenv("WLLM_PARTITION_TOKENS", "256")
+    g = torch.Generator().manual_seed(15)
+    lens = torch.randint(1, 1500, (1100,), generator=g).tolist()
+    case = workloads.custom_case("big_step", lens=lens, num_q_heads=4, num_kv_heads=1, head_dim=64,
+                                 block_size=16, dtype=torch.float16, seed=15)
+    got, kc, vc = fused_step(case)
+    ref, kr, vr = oracle_step(case)
+    assert torch.equal(int_view(kc.cpu()), int_view(kr)), "K append not bit-exact"
+    assert torch.equal(int_view(vc.cpu()), int_view(vr)), "V append not bit-exact"
+    del kc, vc
+    assert_attention_close(got, ref, case.dtype, "1100 sequences, fused step")
+    assert wllm.device_errors() == 0
+
+
 def test_repeated_launches_leave_scheduler_clean():
     case = workloads.custom_case("rep", lens=[3000, 17, 900], num_q_heads=28, num_kv_heads=4,
                                  head_dim=128, block_size=16, dtype=torch.bfloat16, seed=14)

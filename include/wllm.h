@@ -139,7 +139,7 @@ int wllm_reshape_and_cache(const wllm_tensor* key, const wllm_tensor* value,
  * F16/BF16 the partitions of a sequence are merged inside the same
  * (cooperative) launch as soon as all of them are done -- per-sequence
  * counters in the workspace, waits bounded in time -- for batches of up to
- * 1024 query rows (B * Hq), and by a second kernel for larger batches; the
+ * 512 query rows (B * Hq), and by a second kernel for larger batches; the
  * environment variable WLLM_SEPARATE_COMBINE=1 (or 0) forces the second
  * kernel (or the merge inside the launch).  With a
  * caller workspace set (wllm_set_workspace) the call allocates nothing and can

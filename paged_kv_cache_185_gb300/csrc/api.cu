@@ -819,15 +819,17 @@ int run_decode(const DecodeArgs& a, const wllm_tensor* out, const wllm_tensor* q
     if ((rc = collect_device_errors(s, st, "paged_attention_decode"))) return rc;
   }
   // Split partitions are merged inside the (cooperative) launch, overlapped
-  // with the decode, for batches of up to 1024 query rows, and by a second
-  // kernel for larger ones: measured on GB300, merging in the launch is ahead
-  // for few rows with many partitions (long contexts: 256 rows, up to 105
-  // partitions each; 1024 rows of 8-head MQA) and behind for many rows (2048
-  // rows of a TinyLlama-shaped batch, 7168 of a shared-prefix batch, where the
-  // launch's bookkeeping of finished units costs more than a second kernel).
+  // with the decode, for batches of up to 512 query rows, and by a second
+  // kernel (a programmatic dependent of the decode) for larger ones: measured
+  // on GB300, merging in the launch is ahead for few rows with many
+  // partitions (long contexts: 256 rows, up to 128 partitions each, 328.0 vs
+  // 336.3 us) and behind from 1024 rows on (8-head MQA, 1024 rows: 91.3 vs
+  // 87.0 us; TinyLlama-shaped, 2048 rows: 34.6 vs 31.9 us; a shared-prefix
+  // batch, 7168 rows: 180.8 vs 174.8 us), where the launch's bookkeeping of
+  // finished units costs more than a second kernel.
   // WLLM_SEPARATE_COMBINE=1 / 0 forces one or the other.
   const char* sc = std::getenv("WLLM_SEPARATE_COMBINE");
-  const bool separate_kernel = (sc != nullptr && sc[0] != '\0') ? std::strcmp(sc, "0") != 0 : a.B * a.hq > 1024;
+  const bool separate_kernel = (sc != nullptr && sc[0] != '\0') ? std::strcmp(sc, "0") != 0 : a.B * a.hq > 512;
   const DecodePlan first = make_plan(a.dt, std::min<int64_t>(a.B, kPersistentMaxSeqs), a.hq, a.hkv, a.d, a.mb,
                                      a.bs, a.q_bulk_ok, s->num_sms, a.kv_fp8);
   const int64_t slice = first.persistent ? kPersistentMaxSeqs : a.B;

@@ -338,6 +338,73 @@ __device__ __forceinline__ void combine_rows_np(const DecodeParams& p, const int
   }
 }
 
+// One warp's share of a split row's merge: partitions [p0, p1) of query row
+// `row` folded into a running maximum M (log2 domain), a sum `den` of the
+// partitions' sums scaled to M, and the correspondingly scaled sum of their
+// unnormalised outputs (lane: head_dim elements lane*V .. lane*V+V-1).
+// Partials are read through L2 (other CTAs wrote them).
+template <int D>
+__device__ __forceinline__ void merge_part_range(const DecodeParams& p, int row, int p0, int p1, int lane, float& M,
+                                                 float& den, float (&acc)[D / 32]) {
+  constexpr int V = D / 32;
+  constexpr int kBatch = 32 / V;  // partitions whose outputs are loaded together
+  M = -INFINITY;
+  den = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  const int64_t base = static_cast<int64_t>(row) * p.max_parts;
+  for (int c0 = p0; c0 < p1; c0 += 32) {  // one (m, l) per lane
+    const int cnt = min(32, p1 - c0);
+    const float2 w = lane < cnt ? __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + base + c0 + lane)
+                                : make_float2(-INFINITY, 0.f);
+    float mg = w.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mg = fmaxf(mg, __shfl_xor_sync(kFullMask, mg, off));
+    const float Mn = fmaxf(M, mg);
+    const float rescale = M == -INFINITY ? 0.f : exp2f(M - Mn);
+    M = Mn;
+    den *= rescale;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] *= rescale;
+    const float f = lane < cnt ? exp2f(w.x - M) : 0.f;
+    float dsum = f * w.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(kFullMask, dsum, off);
+    den += dsum;
+    for (int j0 = 0; j0 < cnt; j0 += kBatch) {
+      float o[kBatch][V];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (j0 + j < cnt) {
+          const float* src = p.ws_o + (base + c0 + j0 + j) * D + lane * V;
+          if constexpr (V >= 4) {
+#pragma unroll
+            for (int i = 0; i < V; i += 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src + i));
+              o[j][i] = x.x;
+              o[j][i + 1] = x.y;
+              o[j][i + 2] = x.z;
+              o[j][i + 3] = x.w;
+            }
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+            o[j][0] = x.x;
+            o[j][1] = x.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float fp = __shfl_sync(kFullMask, f, (j0 + j) & 31);
+        if (j0 + j < cnt) {
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[i] = fmaf(fp, o[j][i], acc[i]);
+        }
+      }
+    }
+  }
+}
+
 template <typename T, int D, int R>
 __device__ __forceinline__ void combine_rows(const DecodeParams& p, const int (&rows)[R], int lane) {
   const int l_max = p.max_blocks * p.block_size;
@@ -1402,7 +1469,78 @@ __global__ void __launch_bounds__(PShape<T, D, NT, F8>::kThreads) __maxnreg__((P
   // warp in the order they become ready (bounded waits).  The last row of a
   // (sequence, head tile) puts its two counters back to zero.  Every CTA is
   // resident (cooperative launch), so the waits end.
-  if ((flags & kOverlapCombine) && !failed) {
+  // Few rows with many partitions each (every row fits one CTA): CTA c merges
+  // rows c, c + grid, ... with all its warps, each folding a share of the
+  // row's partitions, then combining the shares through shared memory (the
+  // ring, idle now).  A row with 128 partitions is then three batched loads
+  // per warp instead of sixteen for one warp.  Every decision that guards a
+  // barrier is the same for the whole CTA.
+  if ((flags & kOverlapCombine) && B * p.num_q_heads <= static_cast<int>(gridDim.x) && p.max_parts >= 8) {
+    constexpr int NWARP = W + 2;
+    constexpr int V = D / 32;
+    const bool cta_failed = __syncthreads_or(failed ? 1 : 0) != 0;
+    float* red = reinterpret_cast<float*>(ring);  // [NWARP][D + 2]: each warp's (O, M, den)
+    int* flag = reinterpret_cast<int*>(red + NWARP * (D + 2));
+    int* count = p.ws_count;
+    int* rows_done = p.ws_count + B * Z;
+    const int n_rows = B * p.num_q_heads;
+    for (int row = static_cast<int>(blockIdx.x); !cta_failed && row < n_rows; row += static_cast<int>(gridDim.x)) {
+      const int b = row / p.num_q_heads;
+      const int h = row - b * p.num_q_heads;
+      int L = p.context_lens[b];
+      L = L < 0 ? 0 : (L > l_max ? l_max : L);
+      const int np = L == 0 ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+      if (np < 2) continue;  // written by its unit
+      const int kvh = h / p.group;
+      const int tile = (h - kvh * p.group) / HT;
+      const int bz = b * Z + kvh * p.num_head_tiles + tile;
+      const int nh = min(HT, p.group - tile * HT);
+      if (threadIdx.x == 0) {
+        const bool got = counter_wait_bounded(count + bz, np, p.wait_limit_ns);
+        if (!got) atomicOr(p.err, kErrWaitTimeout);
+        *flag = got ? 1 : 0;
+      }
+      __syncthreads();  // the acquire above orders every thread's partial loads below
+      if (*flag == 0) break;
+      const int per = (np + NWARP - 1) / NWARP;
+      const int p0 = min(np, warp * per), p1 = min(np, p0 + per);
+      float M, den, acc[V];
+      merge_part_range<D>(p, row, p0, p1, lane, M, den, acc);
+      float* mine = red + warp * (D + 2);
+#pragma unroll
+      for (int i = 0; i < V; ++i) mine[lane * V + i] = acc[i];
+      if (lane == 0) {
+        mine[D] = M;
+        mine[D + 1] = den;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        float Mt = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) Mt = fmaxf(Mt, red[w * (D + 2) + D]);
+        float o[V], dt = 0.f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) o[i] = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) {
+          const float mw = red[w * (D + 2) + D];
+          const float fw = mw == -INFINITY ? 0.f : exp2f(mw - Mt);
+          dt += fw * red[w * (D + 2) + D + 1];
+#pragma unroll
+          for (int i = 0; i < V; ++i) o[i] = fmaf(fw, red[w * (D + 2) + lane * V + i], o[i]);
+        }
+        const float inv = 1.f / dt;
+        T* orow = reinterpret_cast<T*>(p.out) + b * p.o_sb + static_cast<int64_t>(h) * p.o_sh + lane * V;
+#pragma unroll
+        for (int i = 0; i < V; ++i) orow[i] = from_f32<T>(o[i] * inv);
+        if (lane == 0 && atomicAdd(rows_done + bz, 1) == nh - 1) {  // the tile's last row: counters back to zero
+          count[bz] = 0;
+          rows_done[bz] = 0;
+        }
+      }
+      __syncthreads();  // the shares are read before the next row overwrites them
+    }
+  } else if ((flags & kOverlapCombine) && !failed) {
     const int nw = static_cast<int>(gridDim.x) * (W + 2);
     const int gwarp = static_cast<int>(blockIdx.x) * (W + 2) + warp;
     const int n_rows = B * p.num_q_heads;
